@@ -1,0 +1,430 @@
+#!/usr/bin/env python3
+"""Benchmark: MLA decode over a paged latent KV cache on GB300.
+
+One step = the whole hot path on one batch: the cache write of the batch's new
+tokens (mla_cache_write), the split-KV pass (mla_decode_splitkv) and the LSE
+merge (mla_decode_merge), with the split count from mla_num_kv_splits.  The
+default workload is the DeepSeek-style per-shard decode batch (B=64, H=16,
+head 576 = 512+64, block 64, seq_lens ~ U{1024..4096}, 64 new tokens).
+
+Prints ONE JSON line (rank 0).  Timing: W warm-up steps, then K steps, each
+step bracketed by CUDA events on the launching stream, L2 flushed between steps
+by writing a 256 MiB buffer (outside the events); barrier + synchronize on
+both sides; the max over ranks.  Multi-GPU (torchrun): every rank runs its own
+replica of the batch (no collective on the data path), value = all ranks'
+bytes / max time.
+
+``--impl reference`` times the CPU oracle (the plain fp64 restatement of the
+method) on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def _traffic_record(kernel_src: str, workload: str):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, or None when the kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        with open(kernel_src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        r = rec.get(workload)
+        if r and r.get("kernel_sha256") == sha:
+            return float(r["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"],
+                    "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import mla_paged_kv_concat_gb300 as mla
+    from mla_paged_kv_concat_gb300 import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib = mla.load()
+    w = W.make(args.workload)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    S = 1 if args.deterministic else mla.mla_num_kv_splits(w.max_seq_len, sms)
+    R, P, D, H = w.kv_lora_rank, w.rope_dim, w.head_dim, w.num_heads
+    rows, seqs = w.num_rows, w.num_seqs
+    kvd = mla.MLA_KV_FP8_E4M3 if w.kv_fp8 else mla.MLA_KV_BF16
+
+    # resident device state
+    if w.kv_fp8:
+        cache = torch.from_numpy(w.kv_cache).to(dev)
+    else:
+        cache = torch.from_numpy(w.kv_cache.view(np.int16)).view(torch.bfloat16).to(dev)
+    nb, bs = w.kv_cache.shape[0], w.block_size
+    bstride = bs * D
+    q = w.q.to(dev)
+    bt = torch.from_numpy(w.block_table).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    kv_c, k_pe = w.kv_c.to(dev), w.k_pe.to(dev)
+    slots = torch.from_numpy(w.slot_mapping).to(dev)
+    T = slots.numel()
+    kv_scale = torch.tensor([w.kv_scale], dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    o = torch.empty(rows, H, R, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(rows, H, dtype=torch.float32, device=dev)
+    wsb = mla.mla_decode_workspace_bytes(rows, H, S, R)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = int(stream.cuda_stream)
+    maxb = bt.shape[1]
+
+    def write(kv_c_t, k_pe_t, slots_t):
+        st = lib.mla_cache_write(kv_c_t.data_ptr(), kv_c_t.stride(0), k_pe_t.data_ptr(),
+                                 k_pe_t.stride(0), slots_t.data_ptr(), T, R, P,
+                                 cache.data_ptr(), nb, bs, bstride, kvd,
+                                 kv_scale.data_ptr(), err.data_ptr(), sp)
+        assert st == 0, st
+
+    def stage1(q_t, bt_t, sl_t, o_t, lse_t):
+        st = lib.mla_decode_splitkv(q_t.data_ptr(), q_t.stride(0), q_t.stride(1), rows, H,
+                                    cache.data_ptr(), kvd, nb, bs, bstride, R, P,
+                                    bt_t.data_ptr(), bt_t.stride(0), maxb, sl_t.data_ptr(),
+                                    seqs, w.sm_scale, kv_scale.data_ptr(), S, ws.data_ptr(),
+                                    ws.numel(), o_t.data_ptr(), lse_t.data_ptr(),
+                                    err.data_ptr(), sp, args.path)
+        assert st == 0, st
+
+    def merge(sl_t, o_t, lse_t):
+        st = lib.mla_decode_merge(rows, H, R, sl_t.data_ptr(), seqs, bs, maxb, S,
+                                  ws.data_ptr(), ws.numel(), o_t.data_ptr(),
+                                  lse_t.data_ptr(), sp)
+        assert st == 0, st
+
+    launches_per_step = (1 if T else 0) + 1 + (1 if S > 1 else 0)
+
+    def step_events():
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        write(kv_c, k_pe, slots)
+        e[1].record(stream)
+        stage1(q, bt, sl, o, lse)
+        e[2].record(stream)
+        merge(sl, o, lse)
+        e[3].record(stream)
+        return e
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step_events()
+    torch.cuda.synchronize(dev)
+
+    evs = []
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        for _ in range(args.steps):
+            flush.zero_()
+            evs.append(step_events())
+        torch.cuda.synchronize(dev)
+        barrier()
+    t_write = [e[0].elapsed_time(e[1]) for e in evs]
+    t_s1 = [e[1].elapsed_time(e[2]) for e in evs]
+    t_merge = [e[2].elapsed_time(e[3]) for e in evs]
+    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    total_ms = float(np.sum(t_step))
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    kv_bytes = w.kv_bytes()
+    flops = w.flops()
+    n_units = world * args.steps
+    value = kv_bytes * n_units / (total_ms * 1e-3) / 1e9
+
+    # ---- e2e through the C ABI with host buffers (pinned), copies timed
+    h_q = w.q.pin_memory()
+    h_bt = torch.from_numpy(w.block_table).pin_memory()
+    h_sl = torch.from_numpy(w.seq_lens).pin_memory()
+    h_kvc, h_kpe = w.kv_c.pin_memory(), w.k_pe.pin_memory()
+    h_slots = torch.from_numpy(w.slot_mapping).pin_memory()
+    h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_q, d_bt, d_sl = torch.empty_like(q), torch.empty_like(bt), torch.empty_like(sl)
+    d_kvc, d_kpe, d_slots = torch.empty_like(kv_c), torch.empty_like(k_pe), torch.empty_like(slots)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_bt, h_sl, h_kvc, h_kpe, h_slots))
+    d2h = h_o.numel() * h_o.element_size() + h_lse.numel() * h_lse.element_size()
+
+    def e2e_step():
+        for dst, src in ((d_q, h_q), (d_bt, h_bt), (d_sl, h_sl), (d_kvc, h_kvc),
+                         (d_kpe, h_kpe), (d_slots, h_slots)):
+            dst.copy_(src, non_blocking=True)
+        write(d_kvc, d_kpe, d_slots)
+        st = lib.mla_decode(d_q.data_ptr(), d_q.stride(0), d_q.stride(1), rows, H,
+                            cache.data_ptr(), kvd, nb, bs, bstride, R, P, d_bt.data_ptr(),
+                            d_bt.stride(0), maxb, d_sl.data_ptr(), seqs, w.sm_scale,
+                            kv_scale.data_ptr(), S, ws.data_ptr(), ws.numel(), o.data_ptr(),
+                            lse.data_ptr(), err.data_ptr(), sp)
+        assert st == 0, st
+        h_o.copy_(o, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        e2e_ms.append((a, b))
+    torch.cuda.synchronize(dev)
+    e2e_total = float(sum(a.elapsed_time(b) for a, b in e2e_ms))
+    if dist is not None:
+        t = torch.tensor([e2e_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = kv_bytes * n_units / (e2e_total * 1e-3) / 1e9
+    if int(err.item()) != 0:
+        print(f"warning: device error counter {int(err.item())}", file=sys.stderr)
+
+    if rank != 0:
+        return None
+    hbm, bf16, src = _peaks()
+    s1_ms = float(np.mean(t_s1))
+    achieved = kv_bytes / (s1_ms * 1e-3) / 1e9
+    traffic = _traffic_record(os.path.join(ROOT, "mla_paged_kv_concat_gb300", "csrc",
+                                           "decode_mma.cu"), args.workload)
+    roof_t = max(kv_bytes / (hbm * 1e9), flops / (bf16 * 1e12))
+    line = {
+        "metric": "MLA decode KV GB/s & TFLOPS as % of roofline; decode rows/s at 1 GB300",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if not w.kv_fp8 else "bf16 q / e4m3 cache",
+        "data": "synthetic (seeded N(0,1) bf16; NaN-poisoned unused cache memory)",
+        "config": {
+            "workload": args.workload, "num_seqs": seqs, "rows": rows, "heads": H,
+            "kv_lora_rank": R, "rope_dim": P, "block_size": bs,
+            "seq_lens": [int(w.seq_lens.min()), int(w.seq_lens.max())],
+            "kv_tokens": int(w.seq_lens.sum()), "new_tokens": T, "num_kv_splits": S,
+            "parallelism": f"replicas x{world}", "l2": "flushed between steps (256 MiB write)",
+        },
+        "tflops": round(flops * n_units / (total_ms * 1e-3) / 1e12, 2),
+        "rows_per_s": round(rows * n_units / (total_ms * 1e-3), 1),
+        "step_roofline_frac": round(roof_t / (ms_step * 1e-3), 4),
+        "kernel_ms": {"cache_write": round(float(np.mean(t_write)), 5),
+                      "decode_splitkv": round(s1_ms, 5),
+                      "decode_merge": round(float(np.mean(t_merge)), 5)},
+        "roofline": {"bound": "hbm", "kernel": "decode_splitkv (stage 1)",
+                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": traffic,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs, burst)"},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_total / args.steps, 5)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    return line
+
+
+# ---------------------------------------------------------------- oracle timing
+def oracle_sample(workload: str, n_rows: int):
+    """Time the oracle (as it stands) on the first n_rows rows of the workload:
+    the cache write of those rows' new tokens and the decode of those rows."""
+    import oracle
+    from mla_paged_kv_concat_gb300 import workloads as W
+    w = W.make(workload)
+    n_rows = min(n_rows, w.num_rows)
+    n_seqs = (n_rows + w.rows_per_seq - 1) // w.rows_per_seq
+    n_rows = n_seqs * w.rows_per_seq
+    cache = w.kv_cache.copy()
+    t0 = time.perf_counter()
+    oracle.cache_write(w.kv_c, w.k_pe, w.slot_mapping, cache, block_size=w.block_size,
+                       kv_lora_rank=w.kv_lora_rank, rope_dim=w.rope_dim,
+                       kv_is_fp8=w.kv_fp8, scale=w.kv_scale)
+    oracle.decode(w.q[:n_rows], cache, w.block_table[:n_seqs], w.seq_lens[:n_seqs],
+                  block_size=w.block_size, kv_lora_rank=w.kv_lora_rank, rope_dim=w.rope_dim,
+                  sm_scale=w.sm_scale, kv_is_fp8=w.kv_fp8, kv_scale=w.kv_scale)
+    dt = time.perf_counter() - t0
+    kv = int(w.seq_lens[:n_seqs].astype(np.int64).sum()) * w.head_dim * w.kv_elem_bytes()
+    return kv / dt / 1e9, dt, n_rows, oracle.max_threads(), w
+
+
+def cpu_baseline(workload: str, n_rows: int):
+    gbs, dt, n, cores, w = oracle_sample(workload, n_rows)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{workload}: cache write of all {w.slot_mapping.size} new tokens + "
+                      f"fp64 decode of rows 0..{n - 1} (all {w.num_heads} heads), "
+                      f"{dt:.2f} s wall"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    vals, dts = [], []
+    for i in range(args.warmup + args.steps):
+        gbs, dt, n, cores, w = oracle_sample(args.workload, args.ref_rows)
+        if i >= args.warmup:
+            vals.append(gbs)
+            dts.append(dt)
+    value = float(np.mean(vals))
+    return {
+        "impl": "reference",
+        "metric": "MLA decode KV GB/s & TFLOPS as % of roofline; decode rows/s at 1 GB300",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * float(np.mean(dts)), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload, "rows_sampled": n},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{args.workload}: rows 0..{n - 1} + the cache write, "
+                                   f"per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="per_shard")
+    ap.add_argument("--deterministic", action="store_true", help="num_kv_splits = 1")
+    ap.add_argument("--path", type=int, default=0, help="0 auto, 1 mma.sync, 2 tcgen05")
+    ap.add_argument("--cpu-rows", type=int, default=16,
+                    help="rows of the workload in the oracle's cpu_baseline sample")
+    ap.add_argument("--ref-rows", type=int, default=4,
+                    help="rows per step in the --impl reference sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if line is not None:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_rows)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

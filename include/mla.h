@@ -1,0 +1,249 @@
+/*
+ * mla.h - C ABI of libmla: MLA decode over a paged latent KV cache on GB300
+ * (sm_103a).
+ *
+ * The library implements three steps of multi-head latent attention (MLA)
+ * decode as described on the vLLM pages it restates:
+ *
+ *   [diff] "frozenleaves/vllm compare v0.11.0...mla_cuda_graphs" ("fix TP"),
+ *          a unified diff of vLLM, cited by file section;
+ *   [note] "Triton and MLA: portable attention and multi-head latent
+ *          attention" (vLLM v0.25.1 architecture note), cited by section;
+ *   [api]  "vllm.v1.attention.backends.mla.triton_mla" (API reference),
+ *          TritonMLAMetadataBuilder.
+ *
+ * Conventions shared by every entry point:
+ *   - Every data pointer is DEVICE memory owned by the caller.  The library
+ *     keeps no pointer after a call returns and allocates no device memory.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream).  No call reads device memory on
+ *     the host or synchronises the stream.
+ *   - Arguments are validated on the host before any launch.  A failed check
+ *     returns a non-zero mla_status and launches nothing.  A launch failure
+ *     returns MLA_ERR_CUDA.  Device code never traps: an out-of-range slot or
+ *     block id is skipped (slot) or read as zeros (block id) and counted in
+ *     the optional device counter `err_count`.
+ *   - Strides are in ELEMENTS of the tensor they describe.
+ */
+#ifndef MLA_GB300_MLA_H_
+#define MLA_GB300_MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,         /* null pointer, bad shape/stride/alignment */
+  MLA_ERR_UNSUPPORTED = 2,         /* valid but not implemented combination   */
+  MLA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below the required size */
+  MLA_ERR_CUDA = 4                 /* a CUDA runtime call or launch failed     */
+} mla_status;
+
+/* Element type of the cache.  "auto" in the pages' kv_cache_dtype string is
+ * MLA_KV_BF16 (the cache holds the model's bf16 values unchanged). */
+typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
+
+/* Which stage-1 kernel mla_decode_ex runs.  AUTO picks the fastest kernel
+ * that supports the shape; the others force one (for tests and benchmarks);
+ * a forced kernel that does not support the shape returns
+ * MLA_ERR_UNSUPPORTED. */
+typedef enum {
+  MLA_PATH_AUTO = 0,
+  MLA_PATH_MMA_SYNC = 1, /* warp-level bf16 MMA, any head count            */
+  MLA_PATH_TCGEN05 = 2   /* tcgen05/TMEM kernel for >= 64 heads, bf16 cache */
+} mla_decode_path;
+
+/*
+ * mla_cache_write - write new tokens' latent rows into the paged cache.
+ *
+ * Restates [diff] csrc/cache_kernels.cu, concat_and_cache_mla_kernel and its
+ * host wrapper concat_and_cache_mla (declared in csrc/cache.h).
+ *
+ * For each token t < num_tokens with s = slot_mapping[t]:
+ *   s < 0               padded token (PAD_SLOT_ID = -1): nothing is written;
+ *   s >= num_blocks*bs  skipped and counted in *err_count;
+ *   otherwise           row (s % bs) of block (s / bs) receives
+ *                       [kv_c[t, 0:R] | k_pe[t, 0:P]].
+ * bf16 cache: the bf16 bits are stored unchanged.  fp8 cache: each element
+ * is E4M3(x / *scale), x / *scale an IEEE fp32 division, rounded to nearest
+ * even with finite overflow saturated to +-448 (OCP E4M3, "e4m3fn").
+ *
+ *   kv_c            bf16 [>= num_tokens, kv_lora_rank], row stride
+ *                   kv_c_row_stride (elements), unit column stride.
+ *   k_pe            bf16 [>= num_tokens, rope_dim], row stride
+ *                   k_pe_row_stride; may be a column slice of a wider tensor.
+ *   slot_mapping    int64 [num_tokens].  num_tokens may be smaller than the
+ *                   rows of kv_c/k_pe (CUDA-graph padding, as in the pages).
+ *   kv_lora_rank R  512 or 256.  rope_dim P: 64.
+ *   kv_cache        [num_blocks, block_size, R+P] of bf16 or E4M3 bytes, the
+ *                   start of block b at element b * block_stride
+ *                   (block_stride >= block_size*(R+P); block_stride*elt a
+ *                   multiple of 16 bytes; kv_cache 16-byte aligned).
+ *   block_size      1 .. 1024.
+ *   scale           device float; read only for MLA_KV_FP8_E4M3.
+ *   err_count       device int, may be NULL; incremented per skipped slot.
+ * Duplicate slots in one call race (unspecified winner), as in the pages.
+ */
+mla_status mla_cache_write(const void* kv_c, int64_t kv_c_row_stride,
+                           const void* k_pe, int64_t k_pe_row_stride,
+                           const int64_t* slot_mapping, int num_tokens,
+                           int kv_lora_rank, int rope_dim, void* kv_cache,
+                           int num_blocks, int block_size, int64_t block_stride,
+                           mla_kv_dtype kv_dtype, const float* scale,
+                           int* err_count, void* stream);
+
+/*
+ * mla_num_kv_splits - the split-count rule.
+ *
+ * [note] Key files, _compute_num_kv_splits: the KV split count is taken from
+ * max_seq_len / 512 and capped at sm_count * 2.  Returns
+ * min(ceil(max_seq_len / 512), 2 * sm_count), at least 1.  Batch-invariant
+ * (deterministic) callers pass num_kv_splits = 1 to mla_decode instead
+ * ([note] Data flow, VLLM_BATCH_INVARIANT).
+ */
+int mla_num_kv_splits(int64_t max_seq_len, int sm_count);
+
+/*
+ * mla_decode_workspace_bytes - bytes of fp32 split partials mla_decode needs:
+ * num_rows * num_heads * num_kv_splits * (kv_lora_rank + 1) * 4, or 0 when
+ * num_kv_splits == 1 (the single pass writes o and lse directly).  Same size
+ * as the pages' attn_logits [B, H, S, R+1] fp32 buffer ([note] Data flow;
+ * [api] _reserve_attn_logits_workspace), laid out as o partials
+ * [rows][S][H][R] followed by lse partials [rows][S][H].
+ */
+size_t mla_decode_workspace_bytes(int num_rows, int num_heads,
+                                  int num_kv_splits, int kv_lora_rank);
+
+/*
+ * mla_decode - split-KV MLA decode (stage 1) plus the LSE merge (stage 2).
+ *
+ * Restates [diff] vllm/attention/ops/triton_decode_attention.py
+ * (decode_attention_fwd -> _fwd_grouped_kernel_stage1 -> _fwd_kernel_stage2)
+ * and [note] Data flow (TritonMLAImpl.forward_mqa): MLA decode is MQA over
+ * the latent cache; every head attends to the same cached rows.
+ *
+ * For row r (sequence b = r / (num_rows / num_seqs)), head h, L = seq_lens[b]:
+ *   K_j = cache row of token j (page block_table[b][j / bs], row j % bs),
+ *         dequantised as E4M3 value * *kv_scale for an fp8 cache;
+ *   s_j = sm_scale * sum_{d < R+P} q[r,h,d] K_j[d];
+ *   o[r,h,:] = sum_j softmax(s)_j K_j[0:R]   (V = the kv_c part);
+ *   lse[r,h] = ln sum_j exp(s_j)              (natural log, fp32).
+ * L = 0 gives o = 0 and lse = -inf.  Rows of one sequence are its flattened
+ * non-causal query rows ([api] TritonMLAMetadataBuilder): no causal mask.
+ *
+ *   q               bf16 [num_rows, num_heads, R+P]: row stride q_row_stride,
+ *                   head stride q_head_stride, unit last stride; q and both
+ *                   strides 16-byte aligned.  ([diff] _forward_decode builds
+ *                   it as cat(q_nope, q_pe).)
+ *   num_heads       1 .. 128.
+ *   kv_cache        as in mla_cache_write; block_size one of 16, 32, 64,
+ *                   128, 256.
+ *   kv_lora_rank R  512 or 256; rope_dim P = 64 (head sizes 576 and 320,
+ *                   [note] Boundaries: get_supported_head_sizes).
+ *   block_table     int32 [num_seqs, >= max_blocks_per_seq], row stride
+ *                   block_table_stride.  Entries past a sequence's last
+ *                   page are never read.
+ *   seq_lens        int32 [num_seqs].  Values are clamped to
+ *                   [0, max_blocks_per_seq * block_size]; a clamp counts
+ *                   one error.
+ *   num_seqs        divides num_rows.
+ *   sm_scale        softmax scale applied to q.k.
+ *   kv_scale        device float, read only for an fp8 cache (the same scale
+ *                   for K and V, [note] Data flow: k_scale = v_scale).
+ *                   An fp8 cache needs a bf16 q ([note] Boundaries).
+ *   num_kv_splits   >= 1.  The pages' partition (split s of
+ *                   ceil(L / S) tokens) is an upper bound: the kernel rounds
+ *                   each split up to whole 64-token tiles, so it may use
+ *                   fewer, longer splits.  1 = one sequential pass per row in
+ *                   a fixed order, bitwise deterministic and batch-invariant.
+ *   workspace       device buffer of >= mla_decode_workspace_bytes(...)
+ *                   bytes, 16-byte aligned; may be NULL when
+ *                   num_kv_splits == 1.
+ *   o               bf16 [num_rows, num_heads, R], contiguous.
+ *   lse             fp32 [num_rows, num_heads], contiguous.
+ *   err_count       device int, may be NULL: counts out-of-range block ids
+ *                   and clamped seq_lens; +(1 << 20) if a pipeline wait
+ *                   timed out (the kernel then returns early).
+ * Every mode is run-to-run deterministic (no floating-point atomics).
+ */
+mla_status mla_decode(const void* q, int64_t q_row_stride,
+                      int64_t q_head_stride, int num_rows, int num_heads,
+                      const void* kv_cache, mla_kv_dtype kv_dtype,
+                      int num_blocks, int block_size, int64_t block_stride,
+                      int kv_lora_rank, int rope_dim,
+                      const int32_t* block_table, int64_t block_table_stride,
+                      int max_blocks_per_seq, const int32_t* seq_lens,
+                      int num_seqs, float sm_scale, const float* kv_scale,
+                      int num_kv_splits, void* workspace,
+                      size_t workspace_bytes, void* o, float* lse,
+                      int* err_count, void* stream);
+
+/* mla_decode with an explicit choice of stage-1 kernel (see mla_decode_path).
+ * All arguments otherwise as mla_decode. */
+mla_status mla_decode_ex(const void* q, int64_t q_row_stride,
+                         int64_t q_head_stride, int num_rows, int num_heads,
+                         const void* kv_cache, mla_kv_dtype kv_dtype,
+                         int num_blocks, int block_size, int64_t block_stride,
+                         int kv_lora_rank, int rope_dim,
+                         const int32_t* block_table,
+                         int64_t block_table_stride, int max_blocks_per_seq,
+                         const int32_t* seq_lens, int num_seqs, float sm_scale,
+                         const float* kv_scale, int num_kv_splits,
+                         void* workspace, size_t workspace_bytes, void* o,
+                         float* lse, int* err_count, void* stream,
+                         mla_decode_path path);
+
+/*
+ * mla_decode_splitkv - stage 1 alone: the split-KV pass of mla_decode
+ * ([diff] triton_decode_attention.py, _decode_grouped_att_m_fwd launching
+ * _fwd_grouped_kernel_stage1).  With num_kv_splits == 1 it writes o and lse
+ * directly; otherwise it writes the split partials into `workspace` and
+ * mla_decode_merge must follow on the same stream.  Arguments as
+ * mla_decode_ex.
+ */
+mla_status mla_decode_splitkv(const void* q, int64_t q_row_stride,
+                              int64_t q_head_stride, int num_rows,
+                              int num_heads, const void* kv_cache,
+                              mla_kv_dtype kv_dtype, int num_blocks,
+                              int block_size, int64_t block_stride,
+                              int kv_lora_rank, int rope_dim,
+                              const int32_t* block_table,
+                              int64_t block_table_stride,
+                              int max_blocks_per_seq, const int32_t* seq_lens,
+                              int num_seqs, float sm_scale,
+                              const float* kv_scale, int num_kv_splits,
+                              void* workspace, size_t workspace_bytes, void* o,
+                              float* lse, int* err_count, void* stream,
+                              mla_decode_path path);
+
+/*
+ * mla_decode_merge - stage 2 alone: merge the split partials that
+ * mla_decode_splitkv left in `workspace` into o (bf16) and lse (fp32)
+ * ([diff] triton_decode_attention.py, _decode_softmax_reducev_fwd launching
+ * _fwd_kernel_stage2).  seq_lens, block_size, max_blocks_per_seq and
+ * num_kv_splits must be the values stage 1 was given: the split partition is
+ * recomputed from them.  A no-op returning MLA_OK when num_kv_splits == 1.
+ */
+mla_status mla_decode_merge(int num_rows, int num_heads, int kv_lora_rank,
+                            const int32_t* seq_lens, int num_seqs,
+                            int block_size, int max_blocks_per_seq,
+                            int num_kv_splits, const void* workspace,
+                            size_t workspace_bytes, void* o, float* lse,
+                            void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mla_status_string(mla_status status);
+
+/* Text of the last CUDA error seen by a call on this host thread that
+ * returned MLA_ERR_CUDA, or "" (static per-thread buffer). */
+const char* mla_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_MLA_H_ */

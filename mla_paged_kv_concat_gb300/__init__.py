@@ -1,0 +1,144 @@
+"""MLA decode over a paged latent KV cache, GB300-native (sm_103a).
+
+Thin Python binding over the C ABI of ``libmla.so`` (``include/mla.h``):
+
+* ``mla_cache_write``, ``mla_decode``, ``mla_decode_ex``,
+  ``mla_num_kv_splits``, ``mla_decode_workspace_bytes`` — the C entry points
+  under the same names, taking raw device pointers (ints) and a stream handle.
+* ``cache_write(...)`` and ``decode(...)`` — torch-tensor conveniences that
+  only marshal pointers, strides and the current CUDA stream; every step of
+  the computation runs in the library's CUDA kernels.
+
+PyTorch supplies device memory and streams; nothing here computes the method.
+"""
+from __future__ import annotations
+
+from . import _lib
+from ._lib import (MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_PATH_AUTO, MLA_PATH_MMA_SYNC,
+                   MLA_PATH_TCGEN05, MlaError, load)
+
+__all__ = [
+    "mla_cache_write", "mla_decode", "mla_decode_ex", "mla_num_kv_splits",
+    "mla_decode_workspace_bytes", "cache_write", "decode", "MlaError", "load",
+    "MLA_KV_BF16", "MLA_KV_FP8_E4M3", "MLA_PATH_AUTO", "MLA_PATH_MMA_SYNC",
+    "MLA_PATH_TCGEN05",
+]
+
+
+# ---------------------------------------------------------------- raw C ABI
+def mla_cache_write(*args) -> int:
+    return load().mla_cache_write(*args)
+
+
+def mla_decode(*args) -> int:
+    return load().mla_decode(*args)
+
+
+def mla_decode_ex(*args) -> int:
+    return load().mla_decode_ex(*args)
+
+
+def mla_num_kv_splits(max_seq_len: int, sm_count: int) -> int:
+    return int(load().mla_num_kv_splits(int(max_seq_len), int(sm_count)))
+
+
+def mla_decode_workspace_bytes(num_rows: int, num_heads: int, num_kv_splits: int,
+                               kv_lora_rank: int) -> int:
+    return int(load().mla_decode_workspace_bytes(num_rows, num_heads, num_kv_splits,
+                                                 kv_lora_rank))
+
+
+# ---------------------------------------------------------------- torch glue
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream=None) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _kv_dtype(kv_cache, kv_cache_dtype: str | None) -> int:
+    torch = _torch()
+    if kv_cache_dtype in (None, "auto"):
+        if kv_cache.dtype == torch.bfloat16:
+            return MLA_KV_BF16
+        if kv_cache.dtype in (torch.uint8, torch.float8_e4m3fn):
+            return MLA_KV_FP8_E4M3
+        raise ValueError(f"unsupported cache dtype {kv_cache.dtype}")
+    if kv_cache_dtype in ("fp8", "fp8_e4m3"):
+        return MLA_KV_FP8_E4M3
+    if kv_cache_dtype == "bf16":
+        return MLA_KV_BF16
+    raise ValueError(f"unsupported kv_cache_dtype {kv_cache_dtype!r}")
+
+
+def _cache_geom(kv_cache):
+    """(num_blocks, block_size, D, block_stride) of a [NB, bs, D] cache view."""
+    nb, bs, d = kv_cache.shape
+    assert kv_cache.stride(2) == 1 and kv_cache.stride(1) == d, "cache rows must be dense"
+    return nb, bs, d, kv_cache.stride(0)
+
+
+def cache_write(kv_c, k_pe, kv_cache, slot_mapping, kv_cache_dtype: str | None = None,
+                scale=None, err_count=None, stream=None) -> None:
+    """Write [kv_c | k_pe] rows into ``kv_cache`` at ``slot_mapping`` (in place).
+
+    Same operands as the pages' concat_and_cache_mla(kv_c, k_pe, kv_cache,
+    slot_mapping, kv_cache_dtype, scale); ``scale`` is a device fp32 tensor
+    (fp8 caches only).
+    """
+    kvd = _kv_dtype(kv_cache, kv_cache_dtype)
+    nb, bs, d, bstride = _cache_geom(kv_cache)
+    assert kv_c.stride(1) == 1 and k_pe.stride(1) == 1
+    R, P = kv_c.shape[1], k_pe.shape[1]
+    assert R + P == d
+    st = load().mla_cache_write(
+        kv_c.data_ptr(), kv_c.stride(0), k_pe.data_ptr(), k_pe.stride(0),
+        slot_mapping.data_ptr(), slot_mapping.numel(), R, P, kv_cache.data_ptr(), nb, bs,
+        bstride, kvd, scale.data_ptr() if scale is not None else None,
+        err_count.data_ptr() if err_count is not None else None, _stream_ptr(stream))
+    _lib.check(st, "mla_cache_write")
+
+
+def decode(q, kv_cache, block_table, seq_lens, sm_scale: float, num_kv_splits: int, *,
+           kv_lora_rank: int | None = None, kv_cache_dtype: str | None = None,
+           kv_scale=None, workspace=None, out=None, lse=None, err_count=None,
+           stream=None, path: int = MLA_PATH_AUTO):
+    """MLA decode; returns (o [rows, H, R] bf16, lse [rows, H] fp32).
+
+    ``q`` [rows, H, R+P] bf16; rows = len(seq_lens) * rows_per_seq.
+    ``kv_cache`` [NB, bs, R+P]; ``block_table`` int32 [seqs, max_blocks];
+    ``seq_lens`` int32 [seqs]; ``kv_scale`` device fp32 tensor for fp8 caches;
+    ``workspace`` a device buffer of at least ``mla_decode_workspace_bytes``
+    bytes (allocated here when omitted and needed).
+    """
+    torch = _torch()
+    kvd = _kv_dtype(kv_cache, kv_cache_dtype)
+    nb, bs, d, bstride = _cache_geom(kv_cache)
+    rows, H, dq = q.shape
+    assert dq == d and q.stride(2) == 1
+    R = kv_lora_rank if kv_lora_rank is not None else d - 64
+    P = d - R
+    seqs = seq_lens.numel()
+    if out is None:
+        out = torch.empty(rows, H, R, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty(rows, H, dtype=torch.float32, device=q.device)
+    need = mla_decode_workspace_bytes(rows, H, num_kv_splits, R)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().mla_decode_ex(
+        q.data_ptr(), q.stride(0), q.stride(1), rows, H, kv_cache.data_ptr(), kvd, nb, bs,
+        bstride, R, P, block_table.data_ptr(), block_table.stride(0), block_table.shape[1],
+        seq_lens.data_ptr(), seqs, float(sm_scale),
+        kv_scale.data_ptr() if kv_scale is not None else None, int(num_kv_splits), ws_ptr,
+        ws_bytes, out.data_ptr(), lse.data_ptr(),
+        err_count.data_ptr() if err_count is not None else None, _stream_ptr(stream),
+        int(path))
+    _lib.check(st, "mla_decode")
+    return out, lse

@@ -1,0 +1,48 @@
+// Launch entry points of the device kernels (host side, C++ linkage).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+// Arguments of one decode call after host validation.  Pointers are device
+// memory.  rows = num_seqs * rows_per_seq.
+struct DecodeParams {
+  const uint16_t* q;  // bf16 [rows, H, R+P]
+  int64_t q_row_stride, q_head_stride;
+  int num_rows, num_heads, rows_per_seq, num_seqs;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int max_blocks;
+  const int32_t* seq_lens;
+  int block_size, num_blocks;
+  float sm_scale;
+  const float* kv_scale;  // device; fp8 cache only (else nullptr)
+  int num_splits;
+  float* ws_o;    // [rows][S][H][R] fp32 partial outputs (S > 1)
+  float* ws_lse;  // [rows][S][H] fp32 partial lse (S > 1)
+  uint16_t* o;    // bf16 [rows, H, R]
+  float* lse;     // fp32 [rows, H]
+  int* err_count;
+};
+
+cudaError_t launch_cache_write(const void* kv_c, int64_t kv_c_stride,
+                               const void* k_pe, int64_t k_pe_stride,
+                               const int64_t* slot_mapping, int num_tokens,
+                               int R, int P, void* cache, int num_blocks,
+                               int block_size, int64_t block_stride, bool fp8,
+                               const float* scale, int* err_count,
+                               cudaStream_t stream);
+
+// Stage 1 on warp-level MMA (mma.sync m16n8k16), any head count.  `tmap` is
+// a 3-D tiled tensor map over the cache {R+P, block_size, num_blocks} with a
+// {64, min(block_size, 64), 1} box: 128-byte swizzle for bf16, none for fp8.
+cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap,
+                              int R, bool fp8, cudaStream_t stream);
+
+// Stage 2: LSE merge of the split partials into o (bf16) and lse (fp32).
+cudaError_t launch_merge(const DecodeParams& p, int R, cudaStream_t stream);
+
+}  // namespace mla

@@ -1,0 +1,366 @@
+// C ABI of libmla (declared in include/mla.h): host-side validation, the
+// split-count rule, workspace sizing, tensor-map encoding and dispatch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/mla.h"
+#include "kernels.cuh"
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+mla_status cuda_fail(cudaError_t e) {
+  snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s",
+           cudaGetErrorName(e), cudaGetErrorString(e));
+  return MLA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Tensor map over the cache viewed as {R+P (dims), block_size (rows),
+// num_blocks}: one box is 64 dims x min(block_size, 64) rows of one block.
+// bf16 boxes land 128-byte swizzled (the layout the MMA operand loads read);
+// fp8 boxes land unswizzled, 64 bytes per row.
+mla_status make_cache_tmap(CUtensorMap* map, const void* cache, bool fp8,
+                           int D, int block_size, int num_blocks,
+                           int64_t block_stride) {
+  auto fn = encode_fn();
+  if (!fn) {
+    snprintf(g_last_cuda_error, sizeof g_last_cuda_error,
+             "cuTensorMapEncodeTiled unavailable");
+    return MLA_ERR_CUDA;
+  }
+  const size_t elt = fp8 ? 1 : 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D),
+                        static_cast<cuuint64_t>(block_size),
+                        static_cast<cuuint64_t>(num_blocks)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * elt,
+                           static_cast<cuuint64_t>(block_stride) * elt};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(block_size < 64 ? block_size : 64), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map,
+                  fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  3, const_cast<void*>(cache), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_last_cuda_error, sizeof g_last_cuda_error,
+             "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
+}
+
+bool supported_latent(int R, int P) {
+  return (R == 512 || R == 256) && P == 64;
+}
+
+bool pow2_block(int bs) {
+  return bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "MLA_ERR_WORKSPACE_TOO_SMALL";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+  }
+  return "MLA_ERR_UNKNOWN";
+}
+
+const char* mla_last_cuda_error(void) { return g_last_cuda_error; }
+
+int mla_num_kv_splits(int64_t max_seq_len, int sm_count) {
+  int64_t s = (max_seq_len + 511) / 512;
+  const int64_t cap = 2 * static_cast<int64_t>(sm_count);
+  if (s > cap) s = cap;
+  if (s < 1) s = 1;
+  return static_cast<int>(s);
+}
+
+size_t mla_decode_workspace_bytes(int num_rows, int num_heads,
+                                  int num_kv_splits, int kv_lora_rank) {
+  if (num_rows <= 0 || num_heads <= 0 || num_kv_splits <= 1 ||
+      kv_lora_rank <= 0)
+    return 0;
+  return static_cast<size_t>(num_rows) * num_heads * num_kv_splits *
+         (static_cast<size_t>(kv_lora_rank) + 1) * sizeof(float);
+}
+
+mla_status mla_cache_write(const void* kv_c, int64_t kv_c_row_stride,
+                           const void* k_pe, int64_t k_pe_row_stride,
+                           const int64_t* slot_mapping, int num_tokens,
+                           int kv_lora_rank, int rope_dim, void* kv_cache,
+                           int num_blocks, int block_size, int64_t block_stride,
+                           mla_kv_dtype kv_dtype, const float* scale,
+                           int* err_count, void* stream) {
+  if (num_tokens < 0 || kv_lora_rank <= 0 || rope_dim <= 0 ||
+      num_blocks <= 0 || block_size <= 0 || block_size > 1024)
+    return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3)
+    return MLA_ERR_INVALID_ARG;
+  if (!supported_latent(kv_lora_rank, rope_dim)) return MLA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return MLA_OK;
+  if (!kv_c || !k_pe || !slot_mapping || !kv_cache) return MLA_ERR_INVALID_ARG;
+  const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  if (fp8 && !scale) return MLA_ERR_INVALID_ARG;
+  if (kv_c_row_stride < kv_lora_rank || k_pe_row_stride < rope_dim)
+    return MLA_ERR_INVALID_ARG;
+  const int D = kv_lora_rank + rope_dim;
+  const size_t elt = fp8 ? 1 : 2;
+  if (block_stride < static_cast<int64_t>(block_size) * D ||
+      (block_stride * elt) % 16 != 0 || !aligned16(kv_cache))
+    return MLA_ERR_INVALID_ARG;
+  cudaError_t e = mla::launch_cache_write(
+      kv_c, kv_c_row_stride, k_pe, k_pe_row_stride, slot_mapping, num_tokens,
+      kv_lora_rank, rope_dim, kv_cache, num_blocks, block_size, block_stride,
+      fp8, scale, err_count, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e);
+}
+
+namespace {
+
+// Validates a decode call and fills `p`; returns MLA_OK or the error.
+mla_status prepare_decode(const void* q, int64_t q_row_stride,
+                          int64_t q_head_stride, int num_rows, int num_heads,
+                          const void* kv_cache, mla_kv_dtype kv_dtype,
+                          int num_blocks, int block_size, int64_t block_stride,
+                          int kv_lora_rank, int rope_dim,
+                          const int32_t* block_table,
+                          int64_t block_table_stride, int max_blocks_per_seq,
+                          const int32_t* seq_lens, int num_seqs, float sm_scale,
+                          const float* kv_scale, int num_kv_splits,
+                          void* workspace, size_t workspace_bytes, void* o,
+                          float* lse, int* err_count, mla_decode_path path,
+                          mla::DecodeParams* p) {
+  // ---- shapes
+  if (num_rows < 0 || num_seqs < 0 || num_heads < 1 || num_heads > 128 ||
+      num_blocks <= 0 || block_size <= 0 || max_blocks_per_seq < 1 ||
+      num_kv_splits < 1 || num_kv_splits > 65535)
+    return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3)
+    return MLA_ERR_INVALID_ARG;
+  if (path != MLA_PATH_AUTO && path != MLA_PATH_MMA_SYNC &&
+      path != MLA_PATH_TCGEN05)
+    return MLA_ERR_INVALID_ARG;
+  if (!supported_latent(kv_lora_rank, rope_dim) || !pow2_block(block_size))
+    return MLA_ERR_UNSUPPORTED;
+  if (num_rows == 0) return MLA_OK;
+  if (num_seqs == 0 || num_rows % num_seqs != 0 || num_seqs > 65535)
+    return MLA_ERR_INVALID_ARG;
+  const int D = kv_lora_rank + rope_dim;
+  const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  const size_t elt = fp8 ? 1 : 2;
+  // ---- pointers, strides, alignment
+  if (!q || !kv_cache || !block_table || !seq_lens || !o || !lse)
+    return MLA_ERR_INVALID_ARG;
+  if (fp8 && !kv_scale) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || q_row_stride % 8 != 0 || q_head_stride % 8 != 0 ||
+      q_head_stride < D ||
+      q_row_stride < static_cast<int64_t>(num_heads) * q_head_stride)
+    return MLA_ERR_INVALID_ARG;
+  if (block_stride < static_cast<int64_t>(block_size) * D ||
+      (block_stride * elt) % 16 != 0 || !aligned16(kv_cache))
+    return MLA_ERR_INVALID_ARG;
+  if (block_table_stride < max_blocks_per_seq) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return MLA_ERR_INVALID_ARG;
+  const size_t need = mla_decode_workspace_bytes(num_rows, num_heads,
+                                                 num_kv_splits, kv_lora_rank);
+  if (need > 0) {
+    if (!workspace) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return MLA_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  }
+  // rows_per_seq * heads query vectors per sequence must fit the grid
+  if (static_cast<int64_t>(num_rows / num_seqs) * num_heads > (1 << 24))
+    return MLA_ERR_UNSUPPORTED;
+  if (path == MLA_PATH_TCGEN05) return MLA_ERR_UNSUPPORTED;
+
+  p->q = static_cast<const uint16_t*>(q);
+  p->q_row_stride = q_row_stride;
+  p->q_head_stride = q_head_stride;
+  p->num_rows = num_rows;
+  p->num_heads = num_heads;
+  p->rows_per_seq = num_rows / num_seqs;
+  p->num_seqs = num_seqs;
+  p->block_table = block_table;
+  p->bt_stride = block_table_stride;
+  p->max_blocks = max_blocks_per_seq;
+  p->seq_lens = seq_lens;
+  p->block_size = block_size;
+  p->num_blocks = num_blocks;
+  p->sm_scale = sm_scale;
+  p->kv_scale = fp8 ? kv_scale : nullptr;
+  p->num_splits = num_kv_splits;
+  const size_t n_o = static_cast<size_t>(num_rows) * num_heads * num_kv_splits *
+                     kv_lora_rank;
+  p->ws_o = need ? static_cast<float*>(workspace) : nullptr;
+  p->ws_lse = need ? static_cast<float*>(workspace) + n_o : nullptr;
+  p->o = static_cast<uint16_t*>(o);
+  p->lse = lse;
+  p->err_count = err_count;
+  return MLA_OK;
+}
+
+mla_status run_stage1(const mla::DecodeParams& p, const void* kv_cache,
+                      bool fp8, int R, int block_size, int num_blocks,
+                      int64_t block_stride, cudaStream_t s) {
+  CUtensorMap tmap;
+  mla_status st = make_cache_tmap(&tmap, kv_cache, fp8, R + 64, block_size,
+                                  num_blocks, block_stride);
+  if (st != MLA_OK) return st;
+  cudaError_t e = mla::launch_decode_mma(p, tmap, R, fp8, s);
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+mla_status mla_decode_splitkv(const void* q, int64_t q_row_stride,
+                              int64_t q_head_stride, int num_rows,
+                              int num_heads, const void* kv_cache,
+                              mla_kv_dtype kv_dtype, int num_blocks,
+                              int block_size, int64_t block_stride,
+                              int kv_lora_rank, int rope_dim,
+                              const int32_t* block_table,
+                              int64_t block_table_stride,
+                              int max_blocks_per_seq, const int32_t* seq_lens,
+                              int num_seqs, float sm_scale,
+                              const float* kv_scale, int num_kv_splits,
+                              void* workspace, size_t workspace_bytes, void* o,
+                              float* lse, int* err_count, void* stream,
+                              mla_decode_path path) {
+  mla::DecodeParams p;
+  mla_status st = prepare_decode(
+      q, q_row_stride, q_head_stride, num_rows, num_heads, kv_cache, kv_dtype,
+      num_blocks, block_size, block_stride, kv_lora_rank, rope_dim,
+      block_table, block_table_stride, max_blocks_per_seq, seq_lens, num_seqs,
+      sm_scale, kv_scale, num_kv_splits, workspace, workspace_bytes, o, lse,
+      err_count, path, &p);
+  if (st != MLA_OK || num_rows == 0) return st;
+  return run_stage1(p, kv_cache, kv_dtype == MLA_KV_FP8_E4M3, kv_lora_rank,
+                    block_size, num_blocks, block_stride,
+                    static_cast<cudaStream_t>(stream));
+}
+
+mla_status mla_decode_merge(int num_rows, int num_heads, int kv_lora_rank,
+                            const int32_t* seq_lens, int num_seqs,
+                            int block_size, int max_blocks_per_seq,
+                            int num_kv_splits, const void* workspace,
+                            size_t workspace_bytes, void* o, float* lse,
+                            void* stream) {
+  if (num_rows < 0 || num_heads < 1 || num_heads > 128 || num_seqs < 0 ||
+      block_size <= 0 || max_blocks_per_seq < 1 || num_kv_splits < 1 ||
+      num_kv_splits > 65535)
+    return MLA_ERR_INVALID_ARG;
+  if (kv_lora_rank != 512 && kv_lora_rank != 256) return MLA_ERR_UNSUPPORTED;
+  if (num_rows == 0 || num_kv_splits == 1) return MLA_OK;
+  if (num_seqs == 0 || num_rows % num_seqs != 0) return MLA_ERR_INVALID_ARG;
+  if (!seq_lens || !workspace || !o || !lse || !aligned16(workspace) ||
+      !aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return MLA_ERR_INVALID_ARG;
+  const size_t need = mla_decode_workspace_bytes(num_rows, num_heads,
+                                                 num_kv_splits, kv_lora_rank);
+  if (workspace_bytes < need) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  mla::DecodeParams p = {};
+  p.num_rows = num_rows;
+  p.num_heads = num_heads;
+  p.rows_per_seq = num_rows / num_seqs;
+  p.num_seqs = num_seqs;
+  p.seq_lens = seq_lens;
+  p.block_size = block_size;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_splits = num_kv_splits;
+  const size_t n_o = static_cast<size_t>(num_rows) * num_heads * num_kv_splits *
+                     kv_lora_rank;
+  p.ws_o = static_cast<float*>(const_cast<void*>(workspace));
+  p.ws_lse = p.ws_o + n_o;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  cudaError_t e = mla::launch_merge(p, kv_lora_rank, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e);
+}
+
+mla_status mla_decode_ex(const void* q, int64_t q_row_stride,
+                         int64_t q_head_stride, int num_rows, int num_heads,
+                         const void* kv_cache, mla_kv_dtype kv_dtype,
+                         int num_blocks, int block_size, int64_t block_stride,
+                         int kv_lora_rank, int rope_dim,
+                         const int32_t* block_table,
+                         int64_t block_table_stride, int max_blocks_per_seq,
+                         const int32_t* seq_lens, int num_seqs, float sm_scale,
+                         const float* kv_scale, int num_kv_splits,
+                         void* workspace, size_t workspace_bytes, void* o,
+                         float* lse, int* err_count, void* stream,
+                         mla_decode_path path) {
+  mla::DecodeParams p;
+  mla_status st = prepare_decode(
+      q, q_row_stride, q_head_stride, num_rows, num_heads, kv_cache, kv_dtype,
+      num_blocks, block_size, block_stride, kv_lora_rank, rope_dim,
+      block_table, block_table_stride, max_blocks_per_seq, seq_lens, num_seqs,
+      sm_scale, kv_scale, num_kv_splits, workspace, workspace_bytes, o, lse,
+      err_count, path, &p);
+  if (st != MLA_OK || num_rows == 0) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = run_stage1(p, kv_cache, kv_dtype == MLA_KV_FP8_E4M3, kv_lora_rank,
+                  block_size, num_blocks, block_stride, s);
+  if (st != MLA_OK) return st;
+  if (num_kv_splits > 1) {
+    cudaError_t e = mla::launch_merge(p, kv_lora_rank, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return MLA_OK;
+}
+
+mla_status mla_decode(const void* q, int64_t q_row_stride,
+                      int64_t q_head_stride, int num_rows, int num_heads,
+                      const void* kv_cache, mla_kv_dtype kv_dtype,
+                      int num_blocks, int block_size, int64_t block_stride,
+                      int kv_lora_rank, int rope_dim,
+                      const int32_t* block_table, int64_t block_table_stride,
+                      int max_blocks_per_seq, const int32_t* seq_lens,
+                      int num_seqs, float sm_scale, const float* kv_scale,
+                      int num_kv_splits, void* workspace,
+                      size_t workspace_bytes, void* o, float* lse,
+                      int* err_count, void* stream) {
+  return mla_decode_ex(q, q_row_stride, q_head_stride, num_rows, num_heads,
+                       kv_cache, kv_dtype, num_blocks, block_size, block_stride,
+                       kv_lora_rank, rope_dim, block_table, block_table_stride,
+                       max_blocks_per_seq, seq_lens, num_seqs, sm_scale,
+                       kv_scale, num_kv_splits, workspace, workspace_bytes, o,
+                       lse, err_count, stream, MLA_PATH_AUTO);
+}
+
+}  // extern "C"

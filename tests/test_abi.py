@@ -1,0 +1,100 @@
+"""The C-ABI library loads, exports every entry point that include/mla.h
+declares, and rejects bad arguments on the host before any launch (so these
+run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_paged_kv_concat_gb300 as mla
+from mla_paged_kv_concat_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "mla.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("mla_cache_write", "mla_decode", "mla_num_kv_splits",
+              "mla_decode_workspace_bytes", "mla_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, name
+
+
+def test_split_rule_and_workspace_size(lib):
+    assert mla.mla_num_kv_splits(4096, 152) == 8
+    assert mla.mla_num_kv_splits(0, 152) == 1
+    assert mla.mla_num_kv_splits(10 ** 7, 152) == 304
+    assert mla.mla_decode_workspace_bytes(64, 16, 8, 512) == 64 * 16 * 8 * 513 * 4
+    assert mla.mla_decode_workspace_bytes(64, 16, 1, 512) == 0
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.mla_status_string(code).decode().startswith("MLA_")
+
+
+FAKE = 1 << 12  # an aligned non-null host address; validation never dereferences
+
+
+def _decode_args(**over):
+    a = dict(q=FAKE, qrs=16 * 576, qhs=576, rows=2, H=16, cache=FAKE, kvd=0, nb=8, bs=64,
+             bstride=64 * 576, R=512, P=64, bt=FAKE, bts=4, maxb=4, sl=FAKE, seqs=2,
+             scale=0.07, kvs=None, S=2, ws=FAKE, wsb=10 ** 9, o=FAKE, lse=FAKE, err=None,
+             stream=None, path=0)
+    a.update(over)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1), (dict(cache=None), 1), (dict(o=None), 1), (dict(lse=None), 1),
+    (dict(bt=None), 1), (dict(sl=None), 1),
+    (dict(H=0), 1), (dict(H=129), 1), (dict(S=0), 1), (dict(rows=3), 1),
+    (dict(R=384), 2), (dict(P=32), 2), (dict(bs=48), 2), (dict(bs=8), 2),
+    (dict(bstride=64 * 576 - 8), 1), (dict(q=FAKE + 2), 1), (dict(qhs=500), 1),
+    (dict(kvd=1, kvs=None), 1), (dict(kvd=7), 1), (dict(path=9), 1),
+    (dict(wsb=100), 3), (dict(ws=None), 1), (dict(ws=FAKE + 4), 1),
+    (dict(bts=2), 1),
+])
+def test_decode_rejects_bad_arguments(lib, over, code):
+    assert lib.mla_decode_ex(*_decode_args(**over)) == code
+
+
+def _write_args(**over):
+    a = dict(kv_c=FAKE, kcs=512, k_pe=FAKE, kps=64, slots=FAKE, T=4, R=512, P=64,
+             cache=FAKE, nb=8, bs=64, bstride=64 * 576, kvd=0, scale=None, err=None,
+             stream=None)
+    a.update(over)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(kv_c=None), 1), (dict(slots=None), 1), (dict(cache=None), 1),
+    (dict(T=-1), 1), (dict(R=100), 2), (dict(kvd=1, scale=None), 1),
+    (dict(bstride=100), 1), (dict(cache=FAKE + 8), 1), (dict(kcs=10), 1),
+    (dict(nb=0), 1), (dict(bs=0), 1),
+])
+def test_cache_write_rejects_bad_arguments(lib, over, code):
+    assert lib.mla_cache_write(*_write_args(**over)) == code
+
+
+def test_zero_work_is_ok_without_touching_memory(lib):
+    assert lib.mla_cache_write(*_write_args(T=0, kv_c=None, slots=None)) == 0
+    assert lib.mla_decode_ex(*_decode_args(rows=0)) == 0
