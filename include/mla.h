@@ -235,6 +235,47 @@ mla_status mla_decode_merge(int num_rows, int num_heads, int kv_lora_rank,
                             size_t workspace_bytes, void* o, float* lse,
                             void* stream);
 
+/* Size of the built-in workspace array of mla_decode_noalloc: 32 MiB. */
+#define MLA_NOALLOC_WORKSPACE_BYTES ((size_t)32 << 20)
+
+/*
+ * mla_decode_noalloc - mla_decode without a caller-supplied workspace.
+ *
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that cannot allocate device memory themselves: a plugin inside a host
+ * application that owns every device allocation through its own pool and
+ * forbids direct cudaMalloc, or a latency-critical loop that may not call
+ * cudaMalloc / cudaFree because they can block or synchronise the device.
+ *
+ * Same arguments and results as mla_decode, minus workspace and
+ * workspace_bytes.  The split partials go to a fixed array of
+ * MLA_NOALLOC_WORKSPACE_BYTES bytes inside the library's device image, which
+ * every GPU that loads the library holds until the process exits.  The call
+ * itself allocates nothing.  A call whose partials would not fit
+ * (mla_decode_workspace_bytes(...) > MLA_NOALLOC_WORKSPACE_BYTES) returns
+ * MLA_ERR_WORKSPACE_TOO_SMALL and launches nothing; use fewer splits or
+ * mla_decode with your own workspace.
+ *
+ * The first call on a device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * All calls share the one array: calls whose kernels overlap on the GPU
+ * (other streams, other host threads on the same device) race on it and
+ * must be serialised by the caller.
+ */
+mla_status mla_decode_noalloc(const void* q, int64_t q_row_stride,
+                              int64_t q_head_stride, int num_rows,
+                              int num_heads, const void* kv_cache,
+                              mla_kv_dtype kv_dtype, int num_blocks,
+                              int block_size, int64_t block_stride,
+                              int kv_lora_rank, int rope_dim,
+                              const int32_t* block_table,
+                              int64_t block_table_stride,
+                              int max_blocks_per_seq, const int32_t* seq_lens,
+                              int num_seqs, float sm_scale,
+                              const float* kv_scale, int num_kv_splits,
+                              void* o, float* lse, int* err_count,
+                              void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* mla_status_string(mla_status status);
 

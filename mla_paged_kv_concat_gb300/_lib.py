@@ -47,6 +47,9 @@ SIGNATURES = {
                                   _SZ, _P, _P, _P, _P, _I32]),
     "mla_decode_merge": (_I32, [_I32, _I32, _I32, _P, _I32, _I32, _I32, _I32, _P, _SZ, _P, _P,
                                 _P]),
+    "mla_decode_noalloc": (_I32, [_P, _I64, _I64, _I32, _I32, _P, _I32, _I32, _I32, _I64,
+                                  _I32, _I32, _P, _I64, _I32, _P, _I32, _F32, _P, _I32, _P,
+                                  _P, _P, _P]),
     "mla_status_string": (ctypes.c_char_p, [_I32]),
     "mla_last_cuda_error": (ctypes.c_char_p, []),
 }
