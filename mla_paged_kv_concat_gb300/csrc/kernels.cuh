@@ -42,6 +42,14 @@ cudaError_t launch_cache_write(const void* kv_c, int64_t kv_c_stride,
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap,
                               int R, bool fp8, cudaStream_t stream);
 
+// Stage 1 on tcgen05/TMEM for bf16 caches with R = 512: one 2-CTA cluster per
+// 128 query vectors and group of `split_group` consecutive splits.  `tmap` as
+// above but with a {64, min(block_size, 32), 1} box.
+cudaError_t launch_decode_tc(const DecodeParams& p, const CUtensorMap& tmap,
+                             int split_group, cudaStream_t stream);
+// Consecutive splits the tcgen05 kernel processes per CTA pair.
+int tc_split_group(const DecodeParams& p, int sm_count);
+
 // Stage 2: LSE merge of the split partials into o (bf16) and lse (fp32).
 cudaError_t launch_merge(const DecodeParams& p, int R, cudaStream_t stream);
 

@@ -11,7 +11,9 @@
 // One warp per (row, head); each lane owns R/32 latent columns in 16-byte
 // groups, so every partial row is read with coalesced 512-byte warp loads.
 // The split partition is recomputed from seq_lens exactly as stage 1 chose
-// it, so empty splits are never read.
+// it, so empty splits are never read; a slot whose lse is -inf belongs to a
+// split that stage 1 processed together with the one before it, and holds no
+// output of its own.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -60,7 +62,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   float den = 0.f;
   for (int s = 0; s < ns; ++s) {
     const int64_t rec = rec0 + static_cast<int64_t>(s) * H;
-    const float w = __expf(p.ws_lse[rec] - M);
+    const float ls = p.ws_lse[rec];
+    if (ls == -INFINITY) continue;  // a split fused into its predecessor
+    const float w = __expf(ls - M);
     const float4* src = reinterpret_cast<const float4*>(p.ws_o + rec * R);
 #pragma unroll
     for (int k = 0; k < NV; ++k) {

@@ -41,12 +41,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Tensor map over the cache viewed as {R+P (dims), block_size (rows),
-// num_blocks}: one box is 64 dims x min(block_size, 64) rows of one block.
+// num_blocks}: one box is 64 dims x min(block_size, max_box_rows) rows of one
+// block.
 // bf16 boxes land 128-byte swizzled (the layout the MMA operand loads read);
 // fp8 boxes land unswizzled, 64 bytes per row.
 mla_status make_cache_tmap(CUtensorMap* map, const void* cache, bool fp8,
                            int D, int block_size, int num_blocks,
-                           int64_t block_stride) {
+                           int64_t block_stride, int max_box_rows) {
   auto fn = encode_fn();
   if (!fn) {
     snprintf(g_last_cuda_error, sizeof g_last_cuda_error,
@@ -59,7 +60,8 @@ mla_status make_cache_tmap(CUtensorMap* map, const void* cache, bool fp8,
                         static_cast<cuuint64_t>(num_blocks)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * elt,
                            static_cast<cuuint64_t>(block_stride) * elt};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(block_size < 64 ? block_size : 64), 1};
+  cuuint32_t box[3] = {
+      64, static_cast<cuuint32_t>(block_size < max_box_rows ? block_size : max_box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map,
                   fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
@@ -84,6 +86,23 @@ bool supported_latent(int R, int P) {
 bool pow2_block(int bs) {
   return bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256;
 }
+
+int device_sm_count() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// The tcgen05 kernel covers bf16 caches with a 512-wide latent.
+bool tc_supported(bool fp8, int R) { return !fp8 && R == 512; }
 
 }  // namespace
 
@@ -207,7 +226,8 @@ mla_status prepare_decode(const void* q, int64_t q_row_stride,
   // rows_per_seq * heads query vectors per sequence must fit the grid
   if (static_cast<int64_t>(num_rows / num_seqs) * num_heads > (1 << 24))
     return MLA_ERR_UNSUPPORTED;
-  if (path == MLA_PATH_TCGEN05) return MLA_ERR_UNSUPPORTED;
+  if (path == MLA_PATH_TCGEN05 && !tc_supported(fp8, kv_lora_rank))
+    return MLA_ERR_UNSUPPORTED;
 
   p->q = static_cast<const uint16_t*>(q);
   p->q_row_stride = q_row_stride;
@@ -235,14 +255,28 @@ mla_status prepare_decode(const void* q, int64_t q_row_stride,
   return MLA_OK;
 }
 
+// Stage-1 kernel choice: the tcgen05 kernel when forced, or (AUTO) when it
+// supports the cache and a sequence has at least 128 query vectors to fill
+// its M = 128 tile; the warp-MMA kernel otherwise.
+bool use_tc(const mla::DecodeParams& p, bool fp8, int R, mla_decode_path path) {
+  if (path == MLA_PATH_TCGEN05) return true;
+  if (path == MLA_PATH_MMA_SYNC) return false;
+  return tc_supported(fp8, R) &&
+         static_cast<int64_t>(p.rows_per_seq) * p.num_heads >= 128;
+}
+
 mla_status run_stage1(const mla::DecodeParams& p, const void* kv_cache,
                       bool fp8, int R, int block_size, int num_blocks,
-                      int64_t block_stride, cudaStream_t s) {
+                      int64_t block_stride, mla_decode_path path,
+                      cudaStream_t s) {
   CUtensorMap tmap;
+  const bool tc = use_tc(p, fp8, R, path);
   mla_status st = make_cache_tmap(&tmap, kv_cache, fp8, R + 64, block_size,
-                                  num_blocks, block_stride);
+                                  num_blocks, block_stride, tc ? 32 : 64);
   if (st != MLA_OK) return st;
-  cudaError_t e = mla::launch_decode_mma(p, tmap, R, fp8, s);
+  cudaError_t e =
+      tc ? mla::launch_decode_tc(p, tmap, mla::tc_split_group(p, device_sm_count()), s)
+         : mla::launch_decode_mma(p, tmap, R, fp8, s);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 
@@ -271,7 +305,7 @@ mla_status mla_decode_splitkv(const void* q, int64_t q_row_stride,
       err_count, path, &p);
   if (st != MLA_OK || num_rows == 0) return st;
   return run_stage1(p, kv_cache, kv_dtype == MLA_KV_FP8_E4M3, kv_lora_rank,
-                    block_size, num_blocks, block_stride,
+                    block_size, num_blocks, block_stride, path,
                     static_cast<cudaStream_t>(stream));
 }
 
@@ -335,7 +369,7 @@ mla_status mla_decode_ex(const void* q, int64_t q_row_stride,
   if (st != MLA_OK || num_rows == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = run_stage1(p, kv_cache, kv_dtype == MLA_KV_FP8_E4M3, kv_lora_rank,
-                  block_size, num_blocks, block_stride, s);
+                  block_size, num_blocks, block_stride, path, s);
   if (st != MLA_OK) return st;
   if (num_kv_splits > 1) {
     cudaError_t e = mla::launch_merge(p, kv_lora_rank, s);

@@ -21,7 +21,12 @@ from _helpers import (Dev, assert_close, oracle_cache, oracle_decode, sample_pai
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [mla.MLA_PATH_MMA_SYNC]
+PATHS = [mla.MLA_PATH_MMA_SYNC, mla.MLA_PATH_TCGEN05]
+
+
+def tc_ok(w):
+    """The tcgen05 kernel covers bf16 caches with a 512-wide latent."""
+    return not w.kv_fp8 and w.kv_lora_rank == 512
 
 
 def _run(w, splits, path=mla.MLA_PATH_AUTO, pairs=None, write=True):
@@ -42,6 +47,13 @@ def _run(w, splits, path=mla.MLA_PATH_AUTO, pairs=None, write=True):
 @pytest.mark.parametrize("path", [mla.MLA_PATH_AUTO] + PATHS)
 def test_tiny(cuda_dev, splits, path):
     _run(W.make("tiny"), splits, path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_per_shard_forced_kernel(cuda_dev, path):
+    """Both stage-1 kernels on the H=16 batch, every (row, head) compared."""
+    w = W.make("per_shard")
+    _run(w, mla.mla_num_kv_splits(w.max_seq_len, sm_count()), path)
 
 
 def test_per_shard_full(cuda_dev):
@@ -113,11 +125,25 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("path", [mla.MLA_PATH_AUTO] + PATHS)
 @pytest.mark.parametrize("splits", [1, 3, 16])
 @pytest.mark.parametrize("case", range(len(SMALL)))
-def test_small_shapes(cuda_dev, case, splits):
+def test_small_shapes(cuda_dev, case, splits, path):
     w = W.make_workload(f"small{case}", seed=200 + case, pool_blocks=None, **SMALL[case])
-    _run(w, splits)
+    if path == mla.MLA_PATH_TCGEN05 and not tc_ok(w):
+        pytest.skip("tcgen05 kernel: bf16 cache, R = 512 only")
+    _run(w, splits, path)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_forced_kernel_rejects_what_it_does_not_cover(cuda_dev, path):
+    w = W.make_workload("rej", seed=64, seq_lens=[100], num_heads=16, kv_lora_rank=256)
+    d = Dev(w)
+    if path == mla.MLA_PATH_TCGEN05:
+        with pytest.raises(mla.MlaError):
+            d.decode(2, path=path)
+    else:
+        d.decode(2, path=path)
 
 
 def test_padded_block_stride(cuda_dev):
@@ -147,31 +173,34 @@ def test_split_count_does_not_change_result_beyond_rounding(cuda_dev):
         assert torch.allclose(l, l1, atol=2e-3)
 
 
-def test_repeat_runs_bitwise_equal(cuda_dev):
+@pytest.mark.parametrize("path", PATHS)
+def test_repeat_runs_bitwise_equal(cuda_dev, path):
     w = W.make("per_shard")
     d = Dev(w)
     d.write()
     for S in (1, 8):
-        a = [t.clone() for t in d.decode(S)]
-        b = d.decode(S)
+        a = [t.clone() for t in d.decode(S, path=path)]
+        b = d.decode(S, path=path)
         torch.cuda.synchronize()
         assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_single_pass_is_batch_invariant(cuda_dev):
+@pytest.mark.parametrize("path", PATHS)
+def test_single_pass_is_batch_invariant(cuda_dev, path):
     """With one split, a row's result does not depend on the rest of the batch."""
     w = W.make("per_shard")
     d = Dev(w)
     d.write()
-    o_all, l_all = d.decode(1)
+    o_all, l_all = d.decode(1, path=path)
     for b in (0, 17, 63):
         o_b, l_b = mla.decode(d.q[b:b + 1], d.cache, d.block_table[b:b + 1],
-                              d.seq_lens[b:b + 1], w.sm_scale, 1)
+                              d.seq_lens[b:b + 1], w.sm_scale, 1, path=path)
         torch.cuda.synchronize()
         assert torch.equal(o_b[0], o_all[b]) and torch.equal(l_b[0], l_all[b])
 
 
-def test_physical_block_permutation_is_bitwise_invariant(cuda_dev):
+@pytest.mark.parametrize("path", PATHS)
+def test_physical_block_permutation_is_bitwise_invariant(cuda_dev, path):
     """Moving every block to another physical slot (and rewriting the table)
     leaves the output bit-for-bit unchanged (the paged-layout invariance of
     the pages' test_decode_attention, page size 1 vs 16)."""
@@ -179,12 +208,12 @@ def test_physical_block_permutation_is_bitwise_invariant(cuda_dev):
                         pool_blocks=30)
     d = Dev(w)
     d.write()
-    o1, l1 = [t.clone() for t in d.decode(4)]
+    o1, l1 = [t.clone() for t in d.decode(4, path=path)]
     perm = torch.randperm(30, generator=torch.Generator().manual_seed(0)).cuda()
     new_cache = torch.empty_like(d.cache)
     new_cache[perm] = d.cache
     new_bt = perm[d.block_table.long()].int()
-    o2, l2 = mla.decode(d.q, new_cache, new_bt, d.seq_lens, w.sm_scale, 4)
+    o2, l2 = mla.decode(d.q, new_cache, new_bt, d.seq_lens, w.sm_scale, 4, path=path)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
