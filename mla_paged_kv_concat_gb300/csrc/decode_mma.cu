@@ -2,28 +2,40 @@
 //
 // Restates "frozenleaves/vllm compare v0.11.0...mla_cuda_graphs",
 // vllm/attention/ops/triton_decode_attention.py, _fwd_grouped_kernel_stage1:
-// one program per (sequence, head group, split) streams its split's tokens
-// through the block table, computes q.k over the latent and rope parts,
-// scales, runs an online softmax and accumulates P.V with V the latent part
-// of the same row; it emits the normalised split output and its lse.
+// a program streams its split's tokens through the block table, computes q.k
+// over the latent and rope parts, scales, runs an online softmax and
+// accumulates P.V with V the latent part of the same row; it emits the
+// normalised split output and its lse.
 //
 // GB300 design (not the page's):
-//   * One CTA = 16*MT query vectors (heads of one row, or several rows of one
-//     sequence) x one split.  All its query vectors share every KV tile, so a
-//     tile is read from HBM once per CTA.
+//   * A "unit" is 16*MT query vectors of one sequence (heads of one row, or
+//     several rows of one sequence); all of them share every KV tile, so a
+//     tile is read from HBM once per unit.
+//   * Persistent mode (num_kv_splits > 1): one CTA per SM.  The tiles of all
+//     units form one list; each CTA takes an equal contiguous share of it, so
+//     every SM streams the same number of bytes whatever the length mix.  A
+//     CTA's share is cut into segments at unit boundaries; each segment
+//     yields one partial (o, lse) in the unit's next free split slot, and the
+//     first segment of a unit marks the slots it does not use with
+//     lse = -inf.  The producer runs ahead across segment boundaries (Q of
+//     the next segment goes into a second buffer), so the load pipeline never
+//     drains inside a CTA.
+//   * Grid mode (num_kv_splits == 1, and very large batches): one CTA per
+//     (unit, split) as in the pages; with one split the CTA writes o and lse
+//     itself, one sequential pass in a fixed order (batch-invariant).
 //   * A producer warp streams 64-token tiles with TMA (one 3-D box per 64
-//     dims per page, 128-byte swizzle) into a STAGES-deep mbarrier ring; the
-//     box coordinate is the page's block id from the block table.  Block ids
+//     dims per page, 128-byte swizzle) into an mbarrier ring; the box
+//     coordinate is the page's block id from the block table.  Block ids
 //     outside the cache read as zeros (TMA out-of-bounds fill).
 //   * 4*MT consumer warps: S = Q.K^T with each warp owning 16 tokens of the
-//     tile (mma.sync m16n8k16, bf16 in, fp32 accumulate); softmax row maxima
-//     and sums are exchanged through shared memory; P (bf16) goes to shared
+//     tile (mma.sync m16n8k16, bf16 in, fp32 accumulate, four independent
+//     accumulator chains over the 576-long reduction); softmax maxima and
+//     sums are exchanged through shared memory; P (bf16) goes to shared
 //     memory; O += P.V with each warp owning a quarter of the latent columns,
 //     accumulators in registers.
 //   * fp8 (E4M3) tiles are converted exactly to bf16 in shared memory by the
 //     consumers; the dequantisation scale is folded into the score scale and
 //     the final output scale.
-//   * The split partition is the pages' ceil(L/S) rounded up to whole tiles.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -49,19 +61,21 @@ struct MmaCfg {
   static constexpr int TILE = NCH * kBN * 128;  // bf16 tile, bytes
   static constexpr int RAW = NCH * kBN * 64;    // raw fp8 tile, bytes
   static constexpr int STAGE_BYTES = FP8 ? RAW : TILE;
-  static constexpr int STAGES = FP8 ? (R == 512 ? 3 : 4) : (R == 512 ? 2 : 4);
+  static constexpr int STAGES = FP8 ? (R == 512 ? 2 : 4) : (R == 512 ? 2 : 4);
   static constexpr int QBOX = 16 * MT * 128;    // one 64-dim chunk of Q
   static constexpr int QBYTES = NCH * QBOX;
   static constexpr int PPITCH = kBN + 8;        // P row pitch (elements)
   static constexpr int PBYTES = 16 * MT * PPITCH * 2;
   static constexpr int OFF_STAGES = 0;
   static constexpr int OFF_CONV = STAGES * STAGE_BYTES;
-  static constexpr int OFF_Q = OFF_CONV + (FP8 ? TILE : 0);
-  static constexpr int OFF_P = OFF_Q + QBYTES;
+  static constexpr int OFF_Q = OFF_CONV + (FP8 ? TILE : 0);  // two Q buffers
+  static constexpr int OFF_P = OFF_Q + 2 * QBYTES;
   static constexpr int OFF_RED = OFF_P + PBYTES;
   static constexpr int RED_BYTES = 2 * MT * 4 * 16 * 4;
   static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
-  static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8 + 1024;  // + align pad
+  static constexpr int NBARS = 2 * STAGES + 4;
+  static constexpr int OFF_PRE = OFF_BAR + NBARS * 8;
+  static constexpr int SMEM = OFF_PRE + (kMaxPersistUnits + 1) * 4 + 1024;
   static_assert(OFF_Q % 1024 == 0 && QBOX % 1024 == 0, "swizzle alignment");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -84,7 +98,52 @@ __device__ __forceinline__ void e4m3x16_to_bf16(uint4 raw, uint4& lo,
   hi = make_uint4(out[4], out[5], out[6], out[7]);
 }
 
-template <int R, bool FP8, int MT>
+__device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
+  int L = __ldg(p.seq_lens + b);
+  const int Lmax = p.max_blocks * p.block_size;
+  return L < 0 ? 0 : (L > Lmax ? Lmax : L);
+}
+
+// One segment of work: tiles [t_lo, t_hi) of unit (b, g) whose sequence has
+// L tokens; its result goes to split slot `slot` (or straight to o/lse when
+// `direct`); `first` segments also mark slots [nslots, S) unused.
+struct Seg {
+  int b, g, L;
+  int t_lo, t_hi;
+  int slot, nslots;
+  bool first, direct, clamped;
+};
+
+// Persistent schedule, identical in every warp that walks it.
+struct Sched {
+  const int* pre;  // [units + 1] first tile of each unit
+  int units, qblocks, C, lo, hi, c;
+  __device__ int first_unit() const {
+    int a = 0, z = units;  // smallest u with pre[u + 1] > lo
+    while (a < z) {
+      const int m = (a + z) >> 1;
+      if (pre[m + 1] > lo) z = m; else a = m + 1;
+    }
+    return a;
+  }
+  // Fills `s` with the segment of unit `u` (must intersect [lo, hi)).
+  __device__ void seg(const DecodeParams& p, int u, Seg& s) const {
+    s.b = u / qblocks;
+    s.g = u - s.b * qblocks;
+    s.L = clamp_len(p, s.b);
+    s.clamped = __ldg(p.seq_lens + s.b) > p.max_blocks * p.block_size;
+    const int a = max(lo, pre[u]), z = min(hi, pre[u + 1]);
+    s.t_lo = a - pre[u];
+    s.t_hi = z - pre[u];
+    const int cf = pre[u] / C;
+    s.slot = c - cf;
+    s.nslots = (pre[u + 1] - 1) / C - cf + 1;
+    s.first = s.slot == 0;
+    s.direct = false;
+  }
+};
+
+template <int R, bool FP8, int MT, bool PERSIST>
 __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
     decode_mma_kernel(const DecodeParams p,
                       const __grid_constant__ CUtensorMap tmap) {
@@ -96,45 +155,108 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_stage = smem + C::OFF_STAGES;
   uint8_t* s_conv = smem + C::OFF_CONV;
-  uint8_t* s_q = smem + C::OFF_Q;
   uint16_t* s_p = reinterpret_cast<uint16_t*>(smem + C::OFF_P);
   float* red_max = reinterpret_cast<float*>(smem + C::OFF_RED);
   float* red_sum = red_max + MT * 4 * 16;
   uint64_t* bar_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* bar_empty = bar_full + STAGES;
+  uint64_t* q_full = bar_empty + STAGES;
+  uint64_t* q_empty = q_full + 2;
+  int* pre = reinterpret_cast<int*>(smem + C::OFF_PRE);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g_blk = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
   const int H = p.num_heads;
   const int nvec = p.rows_per_seq * H;
-  const int v0 = g_blk * 16 * MT;
+  const int qblocks = ceil_div(nvec, 16 * MT);
   const int S = p.num_splits;
 
-  int L = __ldg(p.seq_lens + b);
-  const int Lmax = p.max_blocks * p.block_size;
-  if (L < 0) L = 0;
-  if (L > Lmax) {
-    if (threadIdx.x == 0 && split == 0 && g_blk == 0 && p.err_count)
-      atomicAdd(p.err_count, 1);
-    L = Lmax;
-  }
-  const int per = L > 0 ? ceil_div(ceil_div(L, S), kBN) * kBN : kBN;
-  const int start = split * per;
-  const int end = min(L, start + per);
-  const int ntiles = start < end ? ceil_div(end - start, kBN) : 0;
-
-  if (ntiles == 0) {
-    if (S == 1 && warp < NCW) {
-      // Empty sequence in single-pass mode: o = 0, lse = -inf.
-      for (int i = threadIdx.x; i < 16 * MT * R; i += NCW * 32) {
-        const int qv = i / R, col = i % R, v = v0 + qv;
-        if (v >= nvec) continue;
-        const int row = b * p.rows_per_seq + v / H, h = v % H;
-        p.o[(static_cast<int64_t>(row) * H + h) * R + col] = 0;
-        if (col == 0) p.lse[static_cast<int64_t>(row) * H + h] = -INFINITY;
+  // ---------------------------------------------------------- schedule
+  Sched sch;
+  int nseg = 0;    // grid mode: 0 or 1 segment
+  Seg gseg;        // grid mode segment
+  if constexpr (PERSIST) {
+    const int units = p.num_seqs * qblocks;
+    // pre[u + 1] = tiles of unit u, then an inclusive scan by warp 0
+    for (int u = threadIdx.x; u < units; u += blockDim.x)
+      pre[u + 1] = ceil_div(clamp_len(p, u / qblocks), kBN);
+    if (threadIdx.x == 0) pre[0] = 0;
+    __syncthreads();
+    if (warp == 0) {
+      int carry = 0, mx = 0;
+      for (int base = 1; base <= units; base += 32) {
+        const int i = base + lane;
+        int v = i <= units ? pre[i] : 0;
+        mx = max(mx, v);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += t;
+        }
+        if (i <= units) pre[i] = v + carry;
+        carry += __shfl_sync(0xffffffffu, v, 31);
       }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0) red_max[0] = __int_as_float(mx);
     }
-    return;
+    __syncthreads();
+    const int total = pre[units];
+    const int max_n = __float_as_int(red_max[0]);
+    int Cc = ceil_div(total, gridDim.x);
+    Cc = max(Cc, ceil_div(max_n, S - 1));  // at most S slots per unit
+    Cc = max(Cc, 1);
+    sch.pre = pre;
+    sch.units = units;
+    sch.qblocks = qblocks;
+    sch.C = Cc;
+    sch.c = blockIdx.x;
+    sch.lo = blockIdx.x * Cc;
+    sch.hi = min(total, sch.lo + Cc);
+    __syncthreads();  // red_max reused below
+    if (sch.lo >= sch.hi) return;
+  } else {
+    gseg.g = blockIdx.x;
+    gseg.b = blockIdx.z;
+    const int split = blockIdx.y;
+    int L = __ldg(p.seq_lens + gseg.b);
+    const int Lmax = p.max_blocks * p.block_size;
+    if (L < 0) L = 0;
+    if (L > Lmax) {
+      if (threadIdx.x == 0 && split == 0 && gseg.g == 0 && p.err_count)
+        atomicAdd(p.err_count, 1);
+      L = Lmax;
+    }
+    gseg.L = L;
+    const int per = L > 0 ? ceil_div(ceil_div(L, S), kBN) * kBN : kBN;
+    const int start = split * per;
+    const int end = min(L, start + per);
+    gseg.t_lo = start / kBN;
+    gseg.t_hi = start < end ? ceil_div(end, kBN) : gseg.t_lo;
+    gseg.slot = split;
+    gseg.nslots = S;
+    gseg.first = false;
+    gseg.direct = S == 1;
+    gseg.clamped = false;  // counted above
+    nseg = gseg.t_hi > gseg.t_lo ? 1 : 0;
+    if (nseg == 0) {
+      if (warp < NCW) {
+        const int v0 = gseg.g * 16 * MT;
+        for (int i = threadIdx.x; i < 16 * MT * R; i += NCW * 32) {
+          const int qv = i / R, col = i % R, v = v0 + qv;
+          if (v >= nvec) continue;
+          const int row = gseg.b * p.rows_per_seq + v / H, h = v % H;
+          if (S == 1) {
+            // Empty sequence in single-pass mode: o = 0, lse = -inf.
+            p.o[(static_cast<int64_t>(row) * H + h) * R + col] = 0;
+            if (col == 0) p.lse[static_cast<int64_t>(row) * H + h] = -INFINITY;
+          } else if (col == 0 && L > 0) {
+            // A split past the end of a non-empty sequence: no partial.
+            p.ws_lse[(static_cast<int64_t>(row) * S + split) * H + h] = -INFINITY;
+          }
+        }
+      }
+      return;
+    }
   }
 
   if (threadIdx.x == 0) {
@@ -142,46 +264,107 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
       mbar_init(&bar_full[i], 1);
       mbar_init(&bar_empty[i], NCW);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 32);  // one cp.async arrival per producer lane
+      mbar_init(&q_empty[i], NCW);
+    }
     fence_mbar_init();
   }
   __syncthreads();
 
+  // Walks the CTA's segments in order, calling f(seg, index).
+  auto for_each_seg = [&](auto&& f) {
+    if constexpr (PERSIST) {
+      int k = 0;
+      for (int u = sch.first_unit(); u < sch.units && sch.pre[u] < sch.hi; ++u) {
+        if (sch.pre[u + 1] <= max(sch.lo, sch.pre[u])) continue;  // empty unit
+        Seg s;
+        sch.seg(p, u, s);
+        if (!f(s, k++)) return;
+      }
+    } else {
+      if (nseg) f(gseg, 0);
+    }
+  };
+
   if (warp == NCW) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmap);
-      const int bs = p.block_size;
-      const int rows_box = bs < kBN ? bs : kBN;
-      const int npg = kBN / rows_box;
-      constexpr int ROWB = FP8 ? 64 : 128;
-      const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-      for (int i = 0; i < ntiles; ++i) {
-        const int st = i % STAGES;
-        const uint32_t ph = (i / STAGES) & 1;
-        if (!mbar_wait(&bar_empty[st], ph ^ 1)) {
-          if (p.err_count) atomicAdd(p.err_count, kTimeoutErr);
-          break;
+    const int bs = p.block_size;
+    const int rows_box = bs < kBN ? bs : kBN;
+    const int npg = kBN / rows_box;
+    constexpr int ROWB = FP8 ? 64 : 128;
+    if (lane == 0) tma_prefetch_desc(&tmap);
+    int it = 0;  // tiles issued so far (ring position)
+    for_each_seg([&](const Seg& sg, int k) -> bool {
+      // Q of this segment -> buffer k & 1 (all lanes), once the consumers are
+      // done with the segment that used it two segments ago.
+      if (!__all_sync(0xffffffffu, mbar_wait(&q_empty[k & 1], ((k >> 1) & 1) ^ 1))) {
+        if (lane == 0 && p.err_count) atomicAdd(p.err_count, kTimeoutErr);
+        return false;
+      }
+      // cp.async: the copies proceed while this warp goes on issuing tiles;
+      // q_full completes when every lane's copies have landed.
+      const uint32_t s_q = smem_u32(smem + C::OFF_Q + (k & 1) * C::QBYTES);
+      const int v0 = sg.g * 16 * MT;
+      for (int i = lane; i < 16 * MT * (D / 8); i += 32) {
+        const int qr = i / (D / 8), ch = i % (D / 8);
+        const int v = v0 + qr;
+        const uint16_t* src = p.q;
+        if (v < nvec) {
+          const int row = sg.b * p.rows_per_seq + v / H, h = v % H;
+          src = p.q + row * p.q_row_stride + h * p.q_head_stride + ch * 8;
         }
-        const int tok0 = start + i * kBN;
-        int npages = 0;
-        for (int pg = 0; pg < npg; ++pg)
-          if (tok0 + pg * rows_box < end) ++npages;
-        mbar_arrive_expect_tx(&bar_full[st],
-                              static_cast<uint32_t>(npages * NCH * rows_box * ROWB));
-        uint8_t* dst = s_stage + st * C::STAGE_BYTES;
-        for (int pg = 0; pg < npages; ++pg) {
-          const int t = tok0 + pg * rows_box;
-          const int blk = __ldg(bt + t / bs);
-          const int row0 = t % bs;
-          if ((blk < 0 || blk >= p.num_blocks) && p.err_count)
-            atomicAdd(p.err_count, 1);
+        cp_async16(s_q + (ch >> 3) * C::QBOX + sw128(qr, ch & 7), src, v < nvec ? 16u : 0u);
+      }
+      cp_async_arrive(&q_full[k & 1]);
+      if (lane == 0) {
+        const int32_t* bt = p.block_table + static_cast<int64_t>(sg.b) * p.bt_stride;
+        // block ids of the next tile are loaded one tile ahead
+        auto fetch = [&](int t, int (&ids)[4]) {
+#pragma unroll
+          for (int pg = 0; pg < 4; ++pg) {
+            const int tk = t * kBN + pg * rows_box;
+            ids[pg] = (pg < npg && t < sg.t_hi && tk < sg.L) ? __ldg(bt + tk / bs) : 0;
+          }
+        };
+        int cur[4], nxt[4];
+        fetch(sg.t_lo, cur);
+        for (int t = sg.t_lo; t < sg.t_hi; ++t, ++it) {
+          fetch(t + 1, nxt);
+          const int st = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&bar_empty[st], ph ^ 1)) {
+            if (p.err_count) atomicAdd(p.err_count, kTimeoutErr);
+            it = -1;
+            break;
+          }
+          const int tok0 = t * kBN;
+          int npages = 0;
+          for (int pg = 0; pg < npg; ++pg)
+            if (tok0 + pg * rows_box < sg.L) ++npages;
+          mbar_arrive_expect_tx(&bar_full[st],
+                                static_cast<uint32_t>(npages * NCH * rows_box * ROWB));
+          uint8_t* dst = s_stage + st * C::STAGE_BYTES;
+#pragma unroll
+          for (int pg = 0; pg < 4; ++pg) {
+            if (pg >= npages) break;
+            const int tk = tok0 + pg * rows_box;
+            const int blk = cur[pg];
+            const int row0 = tk % bs;
+            if ((blk < 0 || blk >= p.num_blocks) && p.err_count)
+              atomicAdd(p.err_count, 1);
 #pragma unroll 1
-          for (int c = 0; c < NCH; ++c)
-            tma_load_3d(dst + c * (kBN * ROWB) + pg * rows_box * ROWB, &tmap,
-                        &bar_full[st], c * 64, row0, blk);
+            for (int c = 0; c < NCH; ++c)
+              tma_load_3d(dst + c * (kBN * ROWB) + pg * rows_box * ROWB, &tmap,
+                          &bar_full[st], c * 64, row0, blk);
+          }
+#pragma unroll
+          for (int pg = 0; pg < 4; ++pg) cur[pg] = nxt[pg];
         }
       }
-    }
+      it = __shfl_sync(0xffffffffu, it, 0);
+      return it >= 0;
+    });
     return;
   }
 
@@ -189,268 +372,298 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
   const int mt = warp >> 2;   // which 16-vector M tile
   const int q4 = warp & 3;    // token quarter (S) / latent quarter (P.V)
   const int ctid = threadIdx.x;  // 0 .. NCW*32-1
-
-  // Q -> shared, 128-byte swizzled rows of 64 dims; padding vectors are 0.
-  for (int i = ctid; i < 16 * MT * (D / 8); i += NCW * 32) {
-    const int qr = i / (D / 8), ch = i % (D / 8);
-    const int v = v0 + qr;
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (v < nvec) {
-      const int row = b * p.rows_per_seq + v / H, h = v % H;
-      val = __ldg(reinterpret_cast<const uint4*>(
-          p.q + row * p.q_row_stride + h * p.q_head_stride + ch * 8));
-    }
-    *reinterpret_cast<uint4*>(s_q + (ch >> 3) * C::QBOX + sw128(qr, ch & 7)) = val;
-  }
-  named_bar_sync(1, NCW * 32);
-
   const float kv_s = FP8 ? __ldg(p.kv_scale) : 1.0f;
   const float scale_log2 = p.sm_scale * kv_s * kLog2e;
   const int g = lane >> 2, tq = lane & 3;
   const int prow0 = mt * 16 + g;  // this thread's rows in P / the M tile
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
-  float acc[NT][4];
-#pragma unroll
-  for (int n = 0; n < NT; ++n)
-    acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-
-  const uint32_t q_base = smem_u32(s_q);
   const uint32_t p_base = smem_u32(s_p);
-  bool ok = true;
+  int it = 0;  // tiles consumed so far (ring position)
 
-  for (int i = 0; i < ntiles && ok; ++i) {
-    const int st = i % STAGES;
-    const uint32_t ph = (i / STAGES) & 1;
-    const int valid = min(kBN, end - (start + i * kBN));
-    if (!mbar_wait(&bar_full[st], ph)) {
+  for_each_seg([&](const Seg& sg, int k) -> bool {
+    if (!mbar_wait(&q_full[k & 1], (k >> 1) & 1)) {
       if (lane == 0 && p.err_count) atomicAdd(p.err_count, kTimeoutErr);
-      ok = false;
-      break;
+      return false;
     }
-    uint8_t* tile;
-    if constexpr (FP8) {
-      // All warps are done reading the previous converted tile.
-      named_bar_sync(1, NCW * 32);
-      const uint8_t* raw = s_stage + st * C::STAGE_BYTES;
-      for (int idx = ctid; idx < NCH * kBN * 4; idx += NCW * 32) {
-        const int c = idx / (kBN * 4), r = (idx >> 2) % kBN, k = idx & 3;
-        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-        if (r < valid)
-          e4m3x16_to_bf16(
-              *reinterpret_cast<const uint4*>(raw + c * (kBN * 64) + r * 64 + k * 16),
-              lo, hi);
-        uint8_t* dst = s_conv + c * (kBN * 128);
-        *reinterpret_cast<uint4*>(dst + sw128(r, 2 * k)) = lo;
-        *reinterpret_cast<uint4*>(dst + sw128(r, 2 * k + 1)) = hi;
+    const uint32_t q_base = smem_u32(smem + C::OFF_Q + (k & 1) * C::QBYTES);
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+    float acc[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+      acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+
+    for (int t = sg.t_lo; t < sg.t_hi; ++t, ++it) {
+      const int st = it % STAGES;
+      const uint32_t ph = (it / STAGES) & 1;
+      const int valid = min(kBN, sg.L - t * kBN);
+      if (!mbar_wait(&bar_full[st], ph)) {
+        if (lane == 0 && p.err_count) atomicAdd(p.err_count, kTimeoutErr);
+        return false;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_empty[st]);
-      named_bar_sync(1, NCW * 32);
-      tile = s_conv;
-    } else {
-      tile = s_stage + st * C::STAGE_BYTES;
-      if (valid < kBN) {
-        // Rows past the split end may hold anything (other tokens' data,
-        // NaN); zero them so that 0 * row stays 0 in P.V.
-        const int nz = (kBN - valid) * NCH * 8;
-        for (int idx = ctid; idx < nz; idx += NCW * 32) {
-          const int r = valid + idx / (NCH * 8), rem = idx % (NCH * 8);
-          *reinterpret_cast<uint4*>(tile + (rem >> 3) * (kBN * 128) + r * 128 +
-                                    (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
+      uint8_t* tile;
+      if constexpr (FP8) {
+        // All warps are done reading the previous converted tile.
         named_bar_sync(1, NCW * 32);
+        const uint8_t* raw = s_stage + st * C::STAGE_BYTES;
+        for (int idx = ctid; idx < NCH * kBN * 4; idx += NCW * 32) {
+          const int c = idx / (kBN * 4), r = (idx >> 2) % kBN, kq = idx & 3;
+          uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+          if (r < valid)
+            e4m3x16_to_bf16(
+                *reinterpret_cast<const uint4*>(raw + c * (kBN * 64) + r * 64 + kq * 16),
+                lo, hi);
+          uint8_t* dst = s_conv + c * (kBN * 128);
+          *reinterpret_cast<uint4*>(dst + sw128(r, 2 * kq)) = lo;
+          *reinterpret_cast<uint4*>(dst + sw128(r, 2 * kq + 1)) = hi;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_empty[st]);
+        named_bar_sync(1, NCW * 32);
+        tile = s_conv;
+      } else {
+        tile = s_stage + st * C::STAGE_BYTES;
+        if (valid < kBN) {
+          // Rows past the sequence end may hold anything (other tokens'
+          // data, NaN); zero them so that 0 * row stays 0 in P.V.
+          const int nz = (kBN - valid) * NCH * 8;
+          for (int idx = ctid; idx < nz; idx += NCW * 32) {
+            const int r = valid + idx / (NCH * 8), rem = idx % (NCH * 8);
+            *reinterpret_cast<uint4*>(tile + (rem >> 3) * (kBN * 128) + r * 128 +
+                                      (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, NCW * 32);
+        }
       }
-    }
-    const uint32_t t_base = smem_u32(tile);
+      const uint32_t t_base = smem_u32(tile);
 
-    // ---- S = Q K^T for this warp's 16 tokens (two 8-token MMA tiles)
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    {
-      const int j = lane >> 3, r8 = lane & 7;
-      const uint32_t a_row = mt * 16 + (j & 1) * 8 + r8;  // Q row for ldmatrix
-      const uint32_t a_kc = j >> 1;
-      const uint32_t b_row = q4 * 16 + (j >> 1) * 8 + r8;  // K row (token)
-      const uint32_t b_kc = j & 1;
-#pragma unroll 4
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t c64 = ks >> 2, kc = (ks & 3) * 2;
-        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-        ldsm_x4(q_base + c64 * C::QBOX + sw128(a_row, kc + a_kc), a0, a1, a2, a3);
-        ldsm_x4(t_base + c64 * (kBN * 128) + sw128(b_row, kc + b_kc), b0, b1, b2, b3);
-        mma_bf16_16816(sc[0], a0, a1, a2, a3, b0, b1);
-        mma_bf16_16816(sc[1], a0, a1, a2, a3, b2, b3);
+      // ---- S = Q K^T for this warp's 16 tokens (two 8-token MMA tiles),
+      // four independent accumulator chains over the reduction
+      float sc[2][4];
+      {
+        float ch[4][2][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int jn = 0; jn < 2; ++jn)
+            ch[a][jn][0] = ch[a][jn][1] = ch[a][jn][2] = ch[a][jn][3] = 0.f;
+        const int j = lane >> 3, r8 = lane & 7;
+        const uint32_t a_row = mt * 16 + (j & 1) * 8 + r8;  // Q row for ldmatrix
+        const uint32_t a_kc = j >> 1;
+        const uint32_t b_row = q4 * 16 + (j >> 1) * 8 + r8;  // K row (token)
+        const uint32_t b_kc = j & 1;
+#pragma unroll
+        for (int c64 = 0; c64 < NCH; ++c64) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t kc = kk * 2;
+            uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+            ldsm_x4(q_base + c64 * C::QBOX + sw128(a_row, kc + a_kc), a0, a1, a2, a3);
+            ldsm_x4(t_base + c64 * (kBN * 128) + sw128(b_row, kc + b_kc), b0, b1, b2, b3);
+            mma_bf16_16816(ch[kk][0], a0, a1, a2, a3, b0, b1);
+            mma_bf16_16816(ch[kk][1], a0, a1, a2, a3, b2, b3);
+          }
+        }
+#pragma unroll
+        for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            sc[jn][e] = (ch[0][jn][e] + ch[1][jn][e]) + (ch[2][jn][e] + ch[3][jn][e]);
+      }
+
+      // ---- online softmax (log2 domain), rows prow0 and prow0 + 8
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tok = q4 * 16 + jn * 8 + 2 * tq + (e & 1);
+          const float tv = tok < valid ? sc[jn][e] * scale_log2 : -INFINITY;
+          sc[jn][e] = tv;
+          mx[e >> 1] = fmaxf(mx[e >> 1], tv);
+        }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      }
+      if (tq == 0) {
+        red_max[(mt * 4 + q4) * 16 + g] = mx[0];
+        red_max[(mt * 4 + q4) * 16 + g + 8] = mx[1];
+      }
+      named_bar_sync(1, NCW * 32);
+      float m_new[2], alpha[2], ps[2] = {0.f, 0.f};
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float tm = red_max[(mt * 4 + 0) * 16 + g + 8 * r];
+#pragma unroll
+        for (int w = 1; w < 4; ++w)
+          tm = fmaxf(tm, red_max[(mt * 4 + w) * 16 + g + 8 * r]);
+        m_new[r] = fmaxf(m_run[r], tm);
+        alpha[r] = ex2(m_run[r] - m_new[r]);
+      }
+#pragma unroll
+      for (int jn = 0; jn < 2; ++jn) {
+        float pe[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          pe[e] = ex2(sc[jn][e] - m_new[e >> 1]);
+          ps[e >> 1] += pe[e];
+        }
+        const int col = q4 * 16 + jn * 8 + 2 * tq;
+        *reinterpret_cast<uint32_t*>(s_p + prow0 * C::PPITCH + col) =
+            pack_bf16x2(pe[0], pe[1]);
+        *reinterpret_cast<uint32_t*>(s_p + (prow0 + 8) * C::PPITCH + col) =
+            pack_bf16x2(pe[2], pe[3]);
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        ps[r] += __shfl_xor_sync(0xffffffffu, ps[r], 1);
+        ps[r] += __shfl_xor_sync(0xffffffffu, ps[r], 2);
+      }
+      if (tq == 0) {
+        red_sum[(mt * 4 + q4) * 16 + g] = ps[0];
+        red_sum[(mt * 4 + q4) * 16 + g + 8] = ps[1];
+      }
+      named_bar_sync(1, NCW * 32);
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float s_tile = red_sum[(mt * 4 + 0) * 16 + g + 8 * r];
+#pragma unroll
+        for (int w = 1; w < 4; ++w) s_tile += red_sum[(mt * 4 + w) * 16 + g + 8 * r];
+        l_run[r] = l_run[r] * alpha[r] + s_tile;
+        m_run[r] = m_new[r];
+      }
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        acc[n][0] *= alpha[0];
+        acc[n][1] *= alpha[0];
+        acc[n][2] *= alpha[1];
+        acc[n][3] *= alpha[1];
+      }
+
+      // ---- O += P V over this warp's R/4 latent columns
+      {
+        const int j = lane >> 3, r8 = lane & 7;
+        const uint32_t pa_row = mt * 16 + (j & 1) * 8 + r8;
+        const uint32_t pa_col = (j >> 1) * 8;
+        const uint32_t v_tok = (j & 1) * 8 + r8;
+        const uint32_t v_nc = j >> 1;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(p_base + (pa_row * C::PPITCH + kk * 16 + pa_col) * 2, a0, a1, a2, a3);
+          const uint32_t tok = kk * 16 + v_tok;
+#pragma unroll
+          for (int n = 0; n < NT; n += 2) {
+            const uint32_t d8 = (q4 * (R / 4) + n * 8) / 8 + v_nc;  // 8-dim chunk
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(t_base + (d8 >> 3) * (kBN * 128) + sw128(tok, d8 & 7), b0, b1, b2, b3);
+            mma_bf16_16816(acc[n], a0, a1, a2, a3, b0, b1);
+            mma_bf16_16816(acc[n + 1], a0, a1, a2, a3, b2, b3);
+          }
+        }
+      }
+      if constexpr (!FP8) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_empty[st]);
       }
     }
 
-    // ---- online softmax (log2 domain), rows prow0 and prow0 + 8
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int jn = 0; jn < 2; ++jn)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tok = q4 * 16 + jn * 8 + 2 * tq + (e & 1);
-        const float t = tok < valid ? sc[jn][e] * scale_log2 : -INFINITY;
-        sc[jn][e] = t;
-        mx[e >> 1] = fmaxf(mx[e >> 1], t);
-      }
+    // ---- segment epilogue: normalise and write (final o/lse, or a partial)
+    const int v0 = sg.g * 16 * MT;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-    }
-    if (tq == 0) {
-      red_max[(mt * 4 + q4) * 16 + g] = mx[0];
-      red_max[(mt * 4 + q4) * 16 + g + 8] = mx[1];
-    }
-    named_bar_sync(1, NCW * 32);
-    float m_new[2], alpha[2], ps[2] = {0.f, 0.f};
+      const int v = v0 + prow0 + 8 * r;
+      if (v >= nvec) continue;
+      const int row = sg.b * p.rows_per_seq + v / H, h = v % H;
+      const float inv = kv_s / l_run[r];
+      float lse2;
+      asm("lg2.approx.f32 %0, %1;" : "=f"(lse2) : "f"(l_run[r]));
+      const float lse = (m_run[r] + lse2) * kLn2;
+      if (sg.direct) {
+        uint16_t* orow = p.o + (static_cast<int64_t>(row) * H + h) * R;
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      float tm = red_max[(mt * 4 + 0) * 16 + g + 8 * r];
+        for (int n = 0; n < NT; ++n) {
+          const int col = q4 * (R / 4) + n * 8 + 2 * tq;
+          *reinterpret_cast<uint32_t*>(orow + col) =
+              pack_bf16x2(acc[n][2 * r] * inv, acc[n][2 * r + 1] * inv);
+        }
+        if (q4 == 0 && tq == 0) p.lse[static_cast<int64_t>(row) * H + h] = lse;
+      } else {
+        const int64_t rec = (static_cast<int64_t>(row) * S + sg.slot) * H + h;
+        float* orow = p.ws_o + rec * R;
 #pragma unroll
-      for (int w = 1; w < 4; ++w)
-        tm = fmaxf(tm, red_max[(mt * 4 + w) * 16 + g + 8 * r]);
-      m_new[r] = fmaxf(m_run[r], tm);
-      alpha[r] = ex2(m_run[r] - m_new[r]);
-    }
-#pragma unroll
-    for (int jn = 0; jn < 2; ++jn) {
-      float pe[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        pe[e] = ex2(sc[jn][e] - m_new[e >> 1]);
-        ps[e >> 1] += pe[e];
-      }
-      const int col = q4 * 16 + jn * 8 + 2 * tq;
-      *reinterpret_cast<uint32_t*>(s_p + prow0 * C::PPITCH + col) =
-          pack_bf16x2(pe[0], pe[1]);
-      *reinterpret_cast<uint32_t*>(s_p + (prow0 + 8) * C::PPITCH + col) =
-          pack_bf16x2(pe[2], pe[3]);
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      ps[r] += __shfl_xor_sync(0xffffffffu, ps[r], 1);
-      ps[r] += __shfl_xor_sync(0xffffffffu, ps[r], 2);
-    }
-    if (tq == 0) {
-      red_sum[(mt * 4 + q4) * 16 + g] = ps[0];
-      red_sum[(mt * 4 + q4) * 16 + g + 8] = ps[1];
-    }
-    named_bar_sync(1, NCW * 32);
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      float s_tile = red_sum[(mt * 4 + 0) * 16 + g + 8 * r];
-#pragma unroll
-      for (int w = 1; w < 4; ++w) s_tile += red_sum[(mt * 4 + w) * 16 + g + 8 * r];
-      l_run[r] = l_run[r] * alpha[r] + s_tile;
-      m_run[r] = m_new[r];
-    }
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      acc[n][0] *= alpha[0];
-      acc[n][1] *= alpha[0];
-      acc[n][2] *= alpha[1];
-      acc[n][3] *= alpha[1];
-    }
-
-    // ---- O += P V over this warp's R/4 latent columns
-    {
-      const int j = lane >> 3, r8 = lane & 7;
-      const uint32_t pa_row = mt * 16 + (j & 1) * 8 + r8;
-      const uint32_t pa_col = (j >> 1) * 8;
-      const uint32_t v_tok = (j & 1) * 8 + r8;
-      const uint32_t v_nc = j >> 1;
-#pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(p_base + (pa_row * C::PPITCH + kk * 16 + pa_col) * 2, a0, a1, a2, a3);
-        const uint32_t tok = kk * 16 + v_tok;
-#pragma unroll
-        for (int n = 0; n < NT; n += 2) {
-          const uint32_t d8 = (q4 * (R / 4) + n * 8) / 8 + v_nc;  // 8-dim chunk
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(t_base + (d8 >> 3) * (kBN * 128) + sw128(tok, d8 & 7), b0, b1, b2, b3);
-          mma_bf16_16816(acc[n], a0, a1, a2, a3, b0, b1);
-          mma_bf16_16816(acc[n + 1], a0, a1, a2, a3, b2, b3);
+        for (int n = 0; n < NT; ++n) {
+          const int col = q4 * (R / 4) + n * 8 + 2 * tq;
+          *reinterpret_cast<float2*>(orow + col) =
+              make_float2(acc[n][2 * r] * inv, acc[n][2 * r + 1] * inv);
+        }
+        if (q4 == 0 && tq == 0) {
+          p.ws_lse[rec] = lse;
+          if (sg.first)  // slots this unit's partition leaves unused
+            for (int s = sg.nslots; s < S; ++s)
+              p.ws_lse[(static_cast<int64_t>(row) * S + s) * H + h] = -INFINITY;
         }
       }
     }
-    if constexpr (!FP8) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_empty[st]);
-    }
-  }
-  if (!ok) return;
-
-  // ---- epilogue: normalise and write (final o/lse, or split partials)
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int v = v0 + prow0 + 8 * r;
-    if (v >= nvec) continue;
-    const int row = b * p.rows_per_seq + v / H, h = v % H;
-    const float inv = kv_s / l_run[r];
-    float lse2;
-    asm("lg2.approx.f32 %0, %1;" : "=f"(lse2) : "f"(l_run[r]));
-    const float lse = (m_run[r] + lse2) * kLn2;
-    if (S == 1) {
-      uint16_t* orow = p.o + (static_cast<int64_t>(row) * H + h) * R;
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        const int col = q4 * (R / 4) + n * 8 + 2 * tq;
-        *reinterpret_cast<uint32_t*>(orow + col) =
-            pack_bf16x2(acc[n][2 * r] * inv, acc[n][2 * r + 1] * inv);
-      }
-      if (q4 == 0 && tq == 0) p.lse[static_cast<int64_t>(row) * H + h] = lse;
-    } else {
-      const int64_t rec = (static_cast<int64_t>(row) * S + split) * H + h;
-      float* orow = p.ws_o + rec * R;
-#pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        const int col = q4 * (R / 4) + n * 8 + 2 * tq;
-        *reinterpret_cast<float2*>(orow + col) =
-            make_float2(acc[n][2 * r] * inv, acc[n][2 * r + 1] * inv);
-      }
-      if (q4 == 0 && tq == 0) p.ws_lse[rec] = lse;
-    }
-  }
+    if (sg.first && sg.clamped && sg.g == 0 && warp == 0 && lane == 0 && p.err_count)
+      atomicAdd(p.err_count, 1);  // seq_len beyond the block table, once per sequence
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&q_empty[k & 1]);
+    return true;
+  });
 }
 
-template <int R, bool FP8, int MT>
-cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmap,
+template <int R, bool FP8, int MT, bool PERSIST>
+cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmap, int sm_count,
                       cudaStream_t stream) {
   using C = MmaCfg<R, FP8, MT>;
   static bool attr_done = false;  // per instantiation; benign race
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<R, FP8, MT>,
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<R, FP8, MT, PERSIST>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   const int nvec = p.rows_per_seq * p.num_heads;
-  const dim3 grid((nvec + 16 * MT - 1) / (16 * MT), p.num_splits, p.num_seqs);
-  decode_mma_kernel<R, FP8, MT><<<grid, C::NTHREADS, C::SMEM, stream>>>(p, tmap);
+  const int qblocks = (nvec + 16 * MT - 1) / (16 * MT);
+  if constexpr (PERSIST) {
+    decode_mma_kernel<R, FP8, MT, true><<<sm_count, C::NTHREADS, C::SMEM, stream>>>(p, tmap);
+  } else {
+    const dim3 grid(qblocks, p.num_splits, p.num_seqs);
+    decode_mma_kernel<R, FP8, MT, false><<<grid, C::NTHREADS, C::SMEM, stream>>>(p, tmap);
+  }
   return cudaGetLastError();
 }
 
+template <int R, bool FP8, int MT>
+cudaError_t launch_r2(const DecodeParams& p, const CUtensorMap& tmap, int sm_count,
+                      cudaStream_t stream) {
+  const int qblocks = (p.rows_per_seq * p.num_heads + 16 * MT - 1) / (16 * MT);
+  const int64_t units = static_cast<int64_t>(qblocks) * p.num_seqs;
+  if (p.num_splits > 1 && units <= kMaxPersistUnits)
+    return launch_mt<R, FP8, MT, true>(p, tmap, sm_count, stream);
+  return launch_mt<R, FP8, MT, false>(p, tmap, sm_count, stream);
+}
+
 template <int R, bool FP8>
-cudaError_t launch_r(const DecodeParams& p, const CUtensorMap& tmap,
+cudaError_t launch_r(const DecodeParams& p, const CUtensorMap& tmap, int sm_count,
                      cudaStream_t stream) {
   const int nvec = p.rows_per_seq * p.num_heads;
-  if (nvec <= 16) return launch_mt<R, FP8, 1>(p, tmap, stream);
-  return launch_mt<R, FP8, 2>(p, tmap, stream);
+  if (nvec <= 16) return launch_r2<R, FP8, 1>(p, tmap, sm_count, stream);
+  return launch_r2<R, FP8, 2>(p, tmap, sm_count, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap,
-                              int R, bool fp8, cudaStream_t stream) {
-  if (R == 512) return fp8 ? launch_r<512, true>(p, tmap, stream)
-                           : launch_r<512, false>(p, tmap, stream);
-  return fp8 ? launch_r<256, true>(p, tmap, stream)
-             : launch_r<256, false>(p, tmap, stream);
+                              int R, bool fp8, int sm_count, cudaStream_t stream) {
+  if (R == 512) return fp8 ? launch_r<512, true>(p, tmap, sm_count, stream)
+                           : launch_r<512, false>(p, tmap, sm_count, stream);
+  return fp8 ? launch_r<256, true>(p, tmap, sm_count, stream)
+             : launch_r<256, false>(p, tmap, sm_count, stream);
 }
 
 }  // namespace mla

@@ -118,14 +118,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 
   if (ntiles == 0) {
     // Both CTAs of the pair take this branch together.
-    if (S == 1 && threadIdx.x < 128) {
+    if (threadIdx.x < 128) {
       const int v = v0 + threadIdx.x;
       if (v < nvec) {
         const int row = b * p.rows_per_seq + v / H, h = v % H;
-        uint16_t* orow = p.o + (static_cast<int64_t>(row) * H + h) * 512 + rank * 256;
-        for (int c = 0; c < 256; c += 8)
-          *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-        if (rank == 0) p.lse[static_cast<int64_t>(row) * H + h] = -INFINITY;
+        if (S == 1) {
+          // Empty sequence in single-pass mode: o = 0, lse = -inf.
+          uint16_t* orow = p.o + (static_cast<int64_t>(row) * H + h) * 512 + rank * 256;
+          for (int c = 0; c < 256; c += 8)
+            *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+          if (rank == 0) p.lse[static_cast<int64_t>(row) * H + h] = -INFINITY;
+        } else if (L > 0 && rank == 0) {
+          // Splits past the end of a non-empty sequence: no partial.
+          for (int s = s0; s < s1; ++s)
+            p.ws_lse[(static_cast<int64_t>(row) * S + s) * H + h] = -INFINITY;
+        }
       }
     }
     return;
@@ -140,7 +147,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 128);
-      mbar_init(&xs_full[i], 128);
+      mbar_init(&xs_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&pv_done[i], 1);
     }
@@ -151,21 +158,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     tc::tmem_alloc(tmem_slot, TMEM_COLS);
     tc::tmem_relinquish();
   }
-  // Q: this CTA's dims of the 128 query vectors, 128-byte swizzled K-major.
+  // Q: this CTA's dims of the 128 query vectors, 128-byte swizzled K-major,
+  // copied with cp.async (padding vectors are zero-filled).
   {
-    uint8_t* s_q = smem + OFF_Q;
+    const uint32_t s_q = smem_u32(smem + OFF_Q);
     const int per_row = nch * 8;  // 16-byte chunks per vector
     for (int i = threadIdx.x; i < 128 * per_row; i += TC_THREADS) {
       const int qr = i / per_row, ch = i % per_row;
       const int v = v0 + qr;
-      uint4 val = make_uint4(0, 0, 0, 0);
+      const uint16_t* src = p.q;
       if (v < nvec) {
         const int row = b * p.rows_per_seq + v / H, h = v % H;
-        val = __ldg(reinterpret_cast<const uint4*>(
-            p.q + row * p.q_row_stride + h * p.q_head_stride + c0 * 64 + ch * 8));
+        src = p.q + row * p.q_row_stride + h * p.q_head_stride + c0 * 64 + ch * 8;
       }
-      *reinterpret_cast<uint4*>(s_q + (ch >> 3) * QCHUNK + sw128(qr, ch & 7)) = val;
+      cp_async16(s_q + (ch >> 3) * QCHUNK + sw128(qr, ch & 7), src, v < nvec ? 16u : 0u);
     }
+    cp_async_wait_all();
   }
   fence_proxy_async_smem();
   tc::fence_before_sync();
@@ -309,14 +317,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       tc::wait_ld();
       tc::fence_before_sync();
       mbar_arrive(&s_free[bb]);
-      // partial S -> the peer's exchange buffer, then tell the peer
+      // partial S -> the peer's exchange buffer with st.async: each store
+      // completes its bytes on the peer's xs_full[bb]; one local thread
+      // announces the 128 x 32 x 4 bytes this CTA expects from the peer.
+      if (row_i == 0) mbar_arrive_expect_tx(&xs_full[bb], 128 * TBN * 4);
       const uint32_t dst = xs_peer + bb * XS_BYTES;
+      const uint32_t pbar = bb ? xsbar_peer1 : xsbar_peer0;
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        tc::st_cluster_v4(dst + j * 16, __uint_as_float(sr[4 * j]),
-                          __uint_as_float(sr[4 * j + 1]), __uint_as_float(sr[4 * j + 2]),
-                          __uint_as_float(sr[4 * j + 3]));
-      tc::mbar_arrive_remote(bb ? xsbar_peer1 : xsbar_peer0);
+        tc::st_async_v4(dst + j * 16, __uint_as_float(sr[4 * j]),
+                        __uint_as_float(sr[4 * j + 1]), __uint_as_float(sr[4 * j + 2]),
+                        __uint_as_float(sr[4 * j + 3]), pbar);
       const bool got = tc::mbar_wait_cluster(&xs_full[bb], u);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       const float* xs = reinterpret_cast<const float*>(smem + OFF_XS + bb * XS_BYTES) +

@@ -7,6 +7,10 @@
 
 namespace mla {
 
+// Largest number of (sequence, 16-vector block) units the persistent
+// warp-MMA schedule handles; larger batches use one CTA per (unit, split).
+constexpr int kMaxPersistUnits = 512;
+
 // Arguments of one decode call after host validation.  Pointers are device
 // memory.  rows = num_seqs * rows_per_seq.
 struct DecodeParams {
@@ -39,8 +43,9 @@ cudaError_t launch_cache_write(const void* kv_c, int64_t kv_c_stride,
 // Stage 1 on warp-level MMA (mma.sync m16n8k16), any head count.  `tmap` is
 // a 3-D tiled tensor map over the cache {R+P, block_size, num_blocks} with a
 // {64, min(block_size, 64), 1} box: 128-byte swizzle for bf16, none for fp8.
+// With num_kv_splits > 1 it runs persistent, one CTA per SM (`sm_count`).
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap,
-                              int R, bool fp8, cudaStream_t stream);
+                              int R, bool fp8, int sm_count, cudaStream_t stream);
 
 // Stage 1 on tcgen05/TMEM for bf16 caches with R = 512: one 2-CTA cluster per
 // 128 query vectors and group of `split_group` consecutive splits.  `tmap` as
@@ -51,6 +56,8 @@ cudaError_t launch_decode_tc(const DecodeParams& p, const CUtensorMap& tmap,
 int tc_split_group(const DecodeParams& p, int sm_count);
 
 // Stage 2: LSE merge of the split partials into o (bf16) and lse (fp32).
+// Every stage-1 kernel leaves, for each (row, head) of a non-empty sequence,
+// every split slot either holding a partial or with lse = -inf.
 cudaError_t launch_merge(const DecodeParams& p, int R, cudaStream_t stream);
 
 }  // namespace mla

@@ -10,10 +10,10 @@
 //
 // One warp per (row, head); each lane owns R/32 latent columns in 16-byte
 // groups, so every partial row is read with coalesced 512-byte warp loads.
-// The split partition is recomputed from seq_lens exactly as stage 1 chose
-// it, so empty splits are never read; a slot whose lse is -inf belongs to a
-// split that stage 1 processed together with the one before it, and holds no
-// output of its own.
+// Stage 1 leaves every split slot of a non-empty sequence either holding a
+// partial or marked with lse = -inf (a slot its partition did not use); the
+// merge visits the slots in index order and skips the marked ones, so it
+// needs no knowledge of how stage 1 partitioned the sequence.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -39,11 +39,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   int L = __ldg(p.seq_lens + row / p.rows_per_seq);
   const int Lmax = p.max_blocks * p.block_size;
   L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
-  const int per = L > 0 ? ((L + S - 1) / S + 63) / 64 * 64 : 64;
-  const int ns = L > 0 ? (L + per - 1) / per : 0;
-
   uint16_t* orow = p.o + static_cast<int64_t>(gw) * R;
-  if (ns == 0) {
+  if (L == 0) {
 #pragma unroll
     for (int k = 0; k < NV; ++k)
       reinterpret_cast<uint2*>(orow)[k * 32 + lane] = make_uint2(0, 0);
@@ -52,7 +49,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   }
   const int64_t rec0 = static_cast<int64_t>(row) * S * H + h;  // split 0
   float M = -INFINITY;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, p.ws_lse[rec0 + static_cast<int64_t>(s) * H]);
+  for (int s = lane; s < S; s += 32) M = fmaxf(M, p.ws_lse[rec0 + static_cast<int64_t>(s) * H]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
@@ -60,10 +57,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
 #pragma unroll
   for (int k = 0; k < NV; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
-  for (int s = 0; s < ns; ++s) {
+  for (int s = 0; s < S; ++s) {
     const int64_t rec = rec0 + static_cast<int64_t>(s) * H;
     const float ls = p.ws_lse[rec];
-    if (ls == -INFINITY) continue;  // a split fused into its predecessor
+    if (ls == -INFINITY) continue;  // a slot stage 1 left without a partial
     const float w = __expf(ls - M);
     const float4* src = reinterpret_cast<const float4*>(p.ws_o + rec * R);
 #pragma unroll

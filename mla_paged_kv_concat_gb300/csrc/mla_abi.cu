@@ -276,7 +276,7 @@ mla_status run_stage1(const mla::DecodeParams& p, const void* kv_cache,
   if (st != MLA_OK) return st;
   cudaError_t e =
       tc ? mla::launch_decode_tc(p, tmap, mla::tc_split_group(p, device_sm_count()), s)
-         : mla::launch_decode_mma(p, tmap, R, fp8, s);
+         : mla::launch_decode_mma(p, tmap, R, fp8, device_sm_count(), s);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 

@@ -151,3 +151,26 @@ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
 }
 
 }  // namespace mla
+
+namespace mla {
+
+// ---------------------------------------------------------------- cp.async
+// 16-byte global -> shared copy; src_bytes < 16 zero-fills the rest (0 = all).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src,
+                                           uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// Arrive on `bar` once this thread's earlier cp.async copies have landed
+// (the arrival is counted in the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+}  // namespace mla

@@ -179,3 +179,21 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 
 }  // namespace tc
 }  // namespace mla
+
+namespace mla {
+namespace tc {
+
+// 16-byte store into another CTA's shared memory that completes `bytes` of
+// the transaction count of the mbarrier at `cluster_bar` (also in that CTA)
+// once the data is there: no fence on either side.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b,
+                                            float c, float d, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], "
+      "{%1, %2, %3, %4}, [%5];" ::"r"(cluster_addr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
+      : "memory");
+}
+
+}  // namespace tc
+}  // namespace mla
