@@ -9,24 +9,32 @@
 //
 // GB300 design.  128 query vectors (one row's 128 heads, or several rows of
 // one sequence) share every KV row, so the work is a dense contraction:
-// S = Q K^T (M=128 vectors, N=32 tokens, K=576) and O = P V (M=128, N=512,
-// K=32).  An fp32 O of 128 x 512 fills all of a CTA's TMEM (512 columns), so
+// S = Q K^T (M=128 vectors, N=64 tokens, K=576) and O = P V (M=128, N=512,
+// K=64).  An fp32 O of 128 x 512 fills all of a CTA's TMEM (512 columns), so
 // the latent dimension is split over a 2-CTA cluster:
 //   rank 0 holds dims [0, 256)   : S partial over them, O[:, 0:256)
 //   rank 1 holds dims [256, 576) : S partial over them, O[:, 256:512)
 // Each CTA loads only its own dims of every KV tile (no byte is read twice),
 // computes its partial S into TMEM, and the two partials are exchanged
-// through distributed shared memory; both CTAs then run the same softmax on
-// S = S_lo + S_hi (identical bits on both sides) and each accumulates its
-// half of O.  Roles per CTA (192 threads):
+// through distributed shared memory (st.async completing on the peer's
+// mbarrier); both CTAs then run the same softmax on S = S_lo + S_hi
+// (identical bits on both sides) and each accumulates its half of O.
+//
+// TMEM (512 columns): O [0, 256), S [256, 320), P [320, 352) as packed
+// bf16, Q [352, 512) as packed bf16 (rank 1 needs 160 columns for its 320
+// dims).  Q and P are A operands read straight from TMEM by the MMAs; only K
+// and V tiles live in shared memory, which leaves room for a 4-stage ring of
+// 64-token tiles (enough bytes in flight to cover the HBM latency).  Tiles
+// are 64 tokens so that each S MMA has N = 64 (an MMA instruction costs
+// about the same to issue up to N = 64).
+//
+// Roles per CTA (192 threads):
 //   warps 0-3  softmax: thread i owns TMEM lane i = query vector i; the
 //              row max / row sum are thread-local; lazy rescaling of O
 //              (only when the running max grows by more than 2^8);
-//   warp 4     TMA producer: 32-token tiles of the paged cache into a
+//   warp 4     TMA producer: 64-token tiles of the paged cache into a
 //              4-stage mbarrier ring (128-byte swizzled boxes);
 //   warp 5     MMA issuer (one thread) and TMEM owner.
-// S is double-buffered in TMEM (S of tile n+1 is computed while the softmax
-// of tile n runs); P is double-buffered in shared memory.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -38,31 +46,29 @@ namespace mla {
 
 namespace {
 
-constexpr int TBN = 32;                   // tokens per tile
+constexpr int TBN = 64;                   // tokens per tile
 constexpr int TSTAGES = 4;                // KV ring depth
 constexpr int TMAXCH = 5;                 // max 64-dim chunks per CTA
-constexpr int CHUNK_BYTES = TBN * 128;    // one 64-dim box of a tile (4 KiB)
+constexpr int CHUNK_BYTES = TBN * 128;    // one 64-dim box of a tile (8 KiB)
 constexpr int STAGE_BYTES = TMAXCH * CHUNK_BYTES;
-constexpr int QCHUNK = 128 * 128;         // 128 vectors x 64 dims (16 KiB)
-constexpr int P_BYTES = 128 * TBN * 2;    // one P tile, bf16
-constexpr int XS_PITCH = TBN + 4;         // floats per exchanged S row
-constexpr int XS_BYTES = 128 * XS_PITCH * 4;
+constexpr int XS_ROW = TBN * 4;           // bytes of one exchanged S row
+constexpr int XS_BYTES = 128 * XS_ROW;
 constexpr int OFF_STAGE = 0;
-constexpr int OFF_Q = OFF_STAGE + TSTAGES * STAGE_BYTES;
-constexpr int OFF_P = OFF_Q + TMAXCH * QCHUNK;
-constexpr int OFF_XS = OFF_P + 2 * P_BYTES;
+constexpr int OFF_XS = OFF_STAGE + TSTAGES * STAGE_BYTES;
 constexpr int OFF_BAR = OFF_XS + 2 * XS_BYTES;
-constexpr int NBARS = 2 * TSTAGES + 5 * 2 + 1;
+constexpr int NBARS = 2 * TSTAGES + 2 + 4 + 1;
 constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
 constexpr int TC_SMEM = OFF_TMEMSLOT + 16 + 1024;  // + alignment slack
 constexpr int TC_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL = 256;  // S buffers at columns 256 + 32*b
+constexpr uint32_t S_COL = 256;  // S, 64 fp32 columns
+constexpr uint32_t P_COL = 320;  // P, 64 bf16 in 32 columns
+constexpr uint32_t Q_COL = 352;  // Q, up to 320 bf16 in 160 columns
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "alignment");
+static_assert(OFF_XS % 1024 == 0, "alignment");
 static_assert(TC_SMEM <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -71,6 +77,12 @@ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   const bool ok = mbar_wait(bar, parity);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Byte offset of 16-byte chunk `c` (0..15) of exchanged S row `r`: the chunk
+// index is XORed with r mod 8 so that 8 consecutive rows hit all 32 banks.
+__device__ __forceinline__ uint32_t xs_off(uint32_t r, uint32_t c) {
+  return r * XS_ROW + ((c ^ (r & 7u)) << 4);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
@@ -82,12 +94,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + TSTAGES;
-  uint64_t* s_full = bars + 2 * TSTAGES;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* xs_full = s_full + 4;
-  uint64_t* p_full = s_full + 6;
-  uint64_t* pv_done = s_full + 8;
-  uint64_t* mma_done = s_full + 10;
+  uint64_t* xs_full = bars + 2 * TSTAGES;  // two exchange buffers
+  uint64_t* s_full = xs_full + 2;
+  uint64_t* s_free = xs_full + 3;
+  uint64_t* p_full = xs_full + 4;
+  uint64_t* pv_done = xs_full + 5;
+  uint64_t* mma_done = xs_full + 6;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEMSLOT);
 
   const uint32_t rank = tc::cluster_ctarank();
@@ -144,13 +156,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
-      mbar_init(&xs_full[i], 1);
-      mbar_init(&p_full[i], 128);
-      mbar_init(&pv_done[i], 1);
-    }
+    for (int i = 0; i < 2; ++i) mbar_init(&xs_full[i], 1);  // expect_tx by one thread
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 128);
+    mbar_init(p_full, 128);
+    mbar_init(pv_done, 1);
     mbar_init(mma_done, 1);
     fence_mbar_init();
   }
@@ -158,32 +168,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     tc::tmem_alloc(tmem_slot, TMEM_COLS);
     tc::tmem_relinquish();
   }
-  // Q: this CTA's dims of the 128 query vectors, 128-byte swizzled K-major,
-  // copied with cp.async (padding vectors are zero-filled).
-  {
-    const uint32_t s_q = smem_u32(smem + OFF_Q);
-    const int per_row = nch * 8;  // 16-byte chunks per vector
-    for (int i = threadIdx.x; i < 128 * per_row; i += TC_THREADS) {
-      const int qr = i / per_row, ch = i % per_row;
-      const int v = v0 + qr;
-      const uint16_t* src = p.q;
-      if (v < nvec) {
-        const int row = b * p.rows_per_seq + v / H, h = v % H;
-        src = p.q + row * p.q_row_stride + h * p.q_head_stride + c0 * 64 + ch * 8;
-      }
-      cp_async16(s_q + (ch >> 3) * QCHUNK + sw128(qr, ch & 7), src, v < nvec ? 16u : 0u);
-    }
-    cp_async_wait_all();
-  }
-  fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
-  tc::cluster_sync();  // the peer's barriers exist before any remote arrive
+  tc::cluster_sync();  // the peer's barriers exist before any remote traffic
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  if (warp < 4) {
+    // Q: thread i puts its vector's dims [64*c0, 64*(c0+nch)) into TMEM lane
+    // i as packed bf16 pairs (padding vectors are zeros).
+    const int v = v0 + threadIdx.x;
+    const uint16_t* src = nullptr;
+    if (v < nvec) {
+      const int row = b * p.rows_per_seq + v / H, h = v % H;
+      src = p.q + row * p.q_row_stride + h * p.q_head_stride + c0 * 64;
+    }
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    for (int c = 0; c < nch; ++c) {
+      uint32_t r[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 x = src ? __ldg(reinterpret_cast<const uint4*>(src + c * 64) + j)
+                            : make_uint4(0, 0, 0, 0);
+        r[4 * j] = x.x;
+        r[4 * j + 1] = x.y;
+        r[4 * j + 2] = x.z;
+        r[4 * j + 3] = x.w;
+      }
+      tc::st_32x32b_x32(tmem + lane_base + Q_COL + c * 32, r);
+    }
+    tc::wait_st();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
   const uint32_t stage_base = smem_u32(smem + OFF_STAGE);
-  const uint32_t q_base = smem_u32(smem + OFF_Q);
-  const uint32_t p_base = smem_u32(smem + OFF_P);
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
@@ -226,22 +244,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     const int nks = nch * 4;
     bool ok = true;
     auto issue_pv = [&](int k) -> bool {
-      if (!warp_wait(&p_full[k & 1], (k >> 1) & 1)) return false;
+      if (!warp_wait(p_full, k & 1)) return false;
       tc::fence_after_sync();
       if (lane == 0) {
         const uint32_t stb = stage_base + (k % TSTAGES) * STAGE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < TBN / 16; ++kk) {
-          // P: K-major, no swizzle, 8x16-byte core matrices (K step 128 B,
-          // M step 512 B); V: MN-major, 128-byte swizzle (N step = next
-          // 64-dim box, K step = 8 tokens = 1024 B).
-          const uint64_t a = tc::smem_desc(p_base + (k & 1) * P_BYTES + kk * 256, 128,
-                                           512, tc::kLayoutNone);
+          // A = P (TMEM, 16 tokens = 8 packed columns per step); B = V:
+          // MN-major, 128-byte swizzle (N step = next 64-dim box, K step =
+          // 8 tokens = 1024 B).
           const uint64_t bd = tc::smem_desc(stb + kk * 2048, CHUNK_BYTES, 1024,
                                             tc::kLayoutSw128);
-          tc::mma_ss(tmem, a, bd, idPV, (k > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_ts(tmem, tmem + P_COL + kk * 8, bd, idPV, (k > 0 || kk > 0) ? 1u : 0u);
         }
-        tc::commit(&pv_done[k & 1]);
+        tc::commit(pv_done);
         tc::commit(&kv_empty[k % TSTAGES]);
       }
       __syncwarp();
@@ -267,22 +283,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      if (n >= 2 && !warp_wait(&s_free[n & 1], ((n - 2) >> 1) & 1)) {
+      if (n >= 1 && !warp_wait(s_free, (n - 1) & 1)) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
       if (lane == 0) {
+        // S = Q K^T: A = Q from TMEM (16 dims = 8 packed columns per step),
+        // B = K tile, K-major with 128-byte swizzle.
         const uint32_t stb = stage_base + st * STAGE_BYTES;
-        const uint32_t dS = tmem + S_COL + (n & 1) * TBN;
         for (int ks = 0; ks < nks; ++ks) {
-          const uint64_t a = tc::smem_desc(q_base + (ks >> 2) * QCHUNK + (ks & 3) * 32, 16,
-                                           1024, tc::kLayoutSw128);
           const uint64_t bd = tc::smem_desc(stb + (ks >> 2) * CHUNK_BYTES + (ks & 3) * 32, 16,
                                             1024, tc::kLayoutSw128);
-          tc::mma_ss(dS, a, bd, idS, ks > 0 ? 1u : 0u);
+          tc::mma_ts(tmem + S_COL, tmem + Q_COL + ks * 8, bd, idS, ks > 0 ? 1u : 0u);
         }
-        tc::commit(&s_full[n & 1]);
+        tc::commit(s_full);
       }
       __syncwarp();
       if (n >= 1 && !issue_pv(n - 1)) {
@@ -300,44 +315,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     const int row_i = threadIdx.x;  // TMEM lane / query vector
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const float scale_log2 = p.sm_scale * kLog2e;
-    const uint32_t xs_local = smem_u32(smem + OFF_XS) + row_i * XS_PITCH * 4;
+    const uint32_t xs_local = smem_u32(smem + OFF_XS);
     const uint32_t xs_peer = tc::map_peer(xs_local, peer);
     const uint32_t xsbar_peer0 = tc::map_peer(smem_u32(&xs_full[0]), peer);
     const uint32_t xsbar_peer1 = tc::map_peer(smem_u32(&xs_full[1]), peer);
-    uint8_t* p_row = smem + OFF_P + (row_i >> 3) * 512 + (row_i & 7) * 16;
     float m_used = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int n = 0; n < ntiles; ++n) {
-      const int bb = n & 1;
-      const uint32_t u = (n >> 1) & 1;
-      if (!warp_wait(&s_full[bb], u)) { ok = false; break; }
+      const int bb = n & 1;             // exchange buffer
+      const uint32_t u = (n >> 1) & 1;  // its phase parity
+      if (!warp_wait(s_full, n & 1)) { ok = false; break; }
       tc::fence_after_sync();
-      uint32_t sr[32];
-      tc::ld_32x32b_x32(tmem + lane_base + S_COL + bb * TBN, sr);
+      uint32_t sr[64];
+      tc::ld_32x32b_x32(tmem + lane_base + S_COL,
+                        *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tc::ld_32x32b_x32(tmem + lane_base + S_COL + 32,
+                        *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tc::wait_ld();
       tc::fence_before_sync();
-      mbar_arrive(&s_free[bb]);
+      mbar_arrive(s_free);
       // partial S -> the peer's exchange buffer with st.async: each store
       // completes its bytes on the peer's xs_full[bb]; one local thread
-      // announces the 128 x 32 x 4 bytes this CTA expects from the peer.
+      // announces the 128 x 64 x 4 bytes this CTA expects from the peer.
       if (row_i == 0) mbar_arrive_expect_tx(&xs_full[bb], 128 * TBN * 4);
-      const uint32_t dst = xs_peer + bb * XS_BYTES;
-      const uint32_t pbar = bb ? xsbar_peer1 : xsbar_peer0;
+      {
+        const uint32_t dst = xs_peer + bb * XS_BYTES;
+        const uint32_t pbar = bb ? xsbar_peer1 : xsbar_peer0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        tc::st_async_v4(dst + j * 16, __uint_as_float(sr[4 * j]),
-                        __uint_as_float(sr[4 * j + 1]), __uint_as_float(sr[4 * j + 2]),
-                        __uint_as_float(sr[4 * j + 3]), pbar);
+        for (int j = 0; j < 16; ++j)
+          tc::st_async_v4(dst + xs_off(row_i, j), __uint_as_float(sr[4 * j]),
+                          __uint_as_float(sr[4 * j + 1]), __uint_as_float(sr[4 * j + 2]),
+                          __uint_as_float(sr[4 * j + 3]), pbar);
+      }
       const bool got = tc::mbar_wait_cluster(&xs_full[bb], u);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-      const float* xs = reinterpret_cast<const float*>(smem + OFF_XS + bb * XS_BYTES) +
-                        row_i * XS_PITCH;
+      const uint8_t* xs = smem + OFF_XS + bb * XS_BYTES;
       const int valid = min(TBN, end - (start + n * TBN));
-      float x[32];
       float mt = -INFINITY;
 #pragma unroll
-      for (int j4 = 0; j4 < 8; ++j4) {
-        const float4 t = *reinterpret_cast<const float4*>(xs + 4 * j4);
+      for (int j4 = 0; j4 < 16; ++j4) {
+        const float4 t = *reinterpret_cast<const float4*>(xs + xs_off(row_i, j4));
         const float tv[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -345,8 +362,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           const float own = __uint_as_float(sr[j]);
           // S = S_lo + S_hi on both CTAs (same operands, same bits)
           const float s = rank == 0 ? own + tv[e] : tv[e] + own;
-          x[j] = j < valid ? s * scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[j]);
+          const float x = j < valid ? s * scale_log2 : -INFINITY;
+          sr[j] = __float_as_uint(x);
+          mt = fmaxf(mt, x);
         }
       }
       const float m_new = fmaxf(m_used, mt);
@@ -354,7 +372,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       if (__any_sync(0xffffffffu, need)) {
         const float alpha = ex2(m_used - m_new);
         if (n > 0) {
-          if (!warp_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1)) { ok = false; break; }
+          if (!warp_wait(pv_done, (n - 1) & 1)) { ok = false; break; }
           tc::fence_after_sync();
 #pragma unroll 1
           for (int c = 0; c < 256; c += 32) {
@@ -370,28 +388,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         l_run *= alpha;
         m_used = m_new;
       }
-      uint32_t pk[16];
+      uint32_t pk[32];
       float psum = 0.f;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float a0 = ex2(x[2 * j] - m_used), a1 = ex2(x[2 * j + 1] - m_used);
+      for (int j = 0; j < 32; ++j) {
+        const float a0 = ex2(__uint_as_float(sr[2 * j]) - m_used);
+        const float a1 = ex2(__uint_as_float(sr[2 * j + 1]) - m_used);
         psum += a0 + a1;
         pk[j] = pack_bf16x2(a0, a1);
       }
       l_run += psum;
-      if (n >= 2 && !warp_wait(&pv_done[bb], ((n - 2) >> 1) & 1)) { ok = false; break; }
-      uint8_t* prow = p_row + bb * P_BYTES;
-#pragma unroll
-      for (int kc = 0; kc < 4; ++kc)
-        *reinterpret_cast<uint4*>(prow + kc * 128) =
-            make_uint4(pk[4 * kc], pk[4 * kc + 1], pk[4 * kc + 2], pk[4 * kc + 3]);
-      fence_proxy_async_smem();
+      // P's TMEM columns are free once the previous P.V has completed
+      if (n >= 1 && !warp_wait(pv_done, (n - 1) & 1)) { ok = false; break; }
+      tc::fence_after_sync();
+      tc::st_32x32b_x32(tmem + lane_base + P_COL, pk);
+      tc::wait_st();
       tc::fence_before_sync();
-      mbar_arrive(&p_full[bb]);
+      mbar_arrive(p_full);
     }
     if (!ok) {
       if (lane == 0 && p.err_count) atomicAdd(p.err_count, kTimeoutErr);
-    } else if (warp_wait(&pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1)) {
+    } else if (warp_wait(pv_done, (ntiles - 1) & 1)) {
       tc::fence_after_sync();
       const int v = v0 + row_i;
       const bool valid_v = v < nvec;
@@ -455,15 +472,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 }  // namespace
 
 int tc_split_group(const DecodeParams& p, int sm_count) {
-  // Fuse consecutive splits so that about two CTA pairs per SM pair are
-  // launched: fewer, longer splits mean fewer partials to write and merge.
+  // Fuse consecutive splits into CTA pairs.  With f splits per pair the
+  // launch has units * ceil(S / f) pairs; the estimated cost (in units of one
+  // split's KV stream) is the number of waves times the work of one pair, plus
+  // the partial outputs each pair writes and the merge reads back (about 0.85
+  // of a split's bytes per 128-vector unit).  Pick f with the lowest cost.
   const int qblocks = (p.rows_per_seq * p.num_heads + 127) / 128;
   const int64_t units = static_cast<int64_t>(qblocks) * p.num_seqs;
-  const int64_t target = sm_count > 1 ? sm_count : 2;  // pairs x 2 waves
-  int64_t groups = (target + units - 1) / units;
-  if (groups < 1) groups = 1;
-  if (groups > p.num_splits) groups = p.num_splits;
-  return static_cast<int>((p.num_splits + groups - 1) / groups);
+  const int64_t pairs = sm_count >= 2 ? sm_count / 2 : 1;
+  const int S = p.num_splits;
+  int best_f = S;
+  double best_cost = 1e300;
+  for (int f = S; f >= 1; --f) {
+    const int64_t groups = (S + f - 1) / f;
+    if (f < S && (S + f) / (f + 1) == groups) continue;  // same grid as f + 1
+    const int64_t ctas = units * groups;
+    const int64_t waves = (ctas + pairs - 1) / pairs;
+    const double cost = static_cast<double>(waves) * f * pairs + 0.85 * ctas;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best_f = f;
+    }
+  }
+  return best_f;
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, const CUtensorMap& tmap,

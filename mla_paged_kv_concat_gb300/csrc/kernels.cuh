@@ -49,7 +49,7 @@ cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap,
 
 // Stage 1 on tcgen05/TMEM for bf16 caches with R = 512: one 2-CTA cluster per
 // 128 query vectors and group of `split_group` consecutive splits.  `tmap` as
-// above but with a {64, min(block_size, 32), 1} box.
+// above ({64, min(block_size, 64), 1} box, 128-byte swizzle).
 cudaError_t launch_decode_tc(const DecodeParams& p, const CUtensorMap& tmap,
                              int split_group, cudaStream_t stream);
 // Consecutive splits the tcgen05 kernel processes per CTA pair.

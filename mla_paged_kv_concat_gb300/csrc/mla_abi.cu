@@ -272,7 +272,7 @@ mla_status run_stage1(const mla::DecodeParams& p, const void* kv_cache,
   CUtensorMap tmap;
   const bool tc = use_tc(p, fp8, R, path);
   mla_status st = make_cache_tmap(&tmap, kv_cache, fp8, R + 64, block_size,
-                                  num_blocks, block_stride, tc ? 32 : 64);
+                                  num_blocks, block_stride, 64);
   if (st != MLA_OK) return st;
   cudaError_t e =
       tc ? mla::launch_decode_tc(p, tmap, mla::tc_split_group(p, device_sm_count()), s)

@@ -197,3 +197,22 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, floa
 
 }  // namespace tc
 }  // namespace mla
+
+namespace mla {
+namespace tc {
+
+// D[tmem] (+)= A[tmem] * B[smem]: A is M lanes x K columns of packed 16-bit
+// pairs (lane m, column k/2, low half = even k); issued by one thread.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem,
+                                       uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+}  // namespace tc
+}  // namespace mla
