@@ -11,6 +11,7 @@
 #include <stdint.h>
 
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace mla {
 
@@ -64,6 +65,9 @@ __device__ __forceinline__ uint8_t quant1(uint16_t bits, float s) {
 template <bool FP8, bool VEC>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
     cache_write_kernel(const CacheWriteArgs a) {
+  // The decode kernels that follow wait for this grid's completion before
+  // they read anything; letting them launch now hides their launch latency.
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   if (t >= a.num_tokens) return;

@@ -75,7 +75,8 @@ struct MmaCfg {
   static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
   static constexpr int NBARS = 2 * STAGES + 4;
   static constexpr int OFF_PRE = OFF_BAR + NBARS * 8;
-  static constexpr int SMEM = OFF_PRE + (kMaxPersistUnits + 1) * 4 + 1024;
+  static constexpr int OFF_LEN = OFF_PRE + (kMaxPersistUnits + 1) * 4;
+  static constexpr int SMEM = OFF_LEN + kMaxPersistUnits * 4 + 1024;
   static_assert(OFF_Q % 1024 == 0 && QBOX % 1024 == 0, "swizzle alignment");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -104,6 +105,8 @@ __device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
   return L < 0 ? 0 : (L > Lmax ? Lmax : L);
 }
 
+constexpr int kClampedBit = 1 << 30;
+
 // One segment of work: tiles [t_lo, t_hi) of unit (b, g) whose sequence has
 // L tokens; its result goes to split slot `slot` (or straight to o/lse when
 // `direct`); `first` segments also mark slots [nslots, S) unused.
@@ -117,6 +120,7 @@ struct Seg {
 // Persistent schedule, identical in every warp that walks it.
 struct Sched {
   const int* pre;  // [units + 1] first tile of each unit
+  const int* len;  // [sequences] clamped length, | kClampedBit if clamped
   int units, qblocks, C, lo, hi, c;
   __device__ int first_unit() const {
     int a = 0, z = units;  // smallest u with pre[u + 1] > lo
@@ -130,8 +134,8 @@ struct Sched {
   __device__ void seg(const DecodeParams& p, int u, Seg& s) const {
     s.b = u / qblocks;
     s.g = u - s.b * qblocks;
-    s.L = clamp_len(p, s.b);
-    s.clamped = __ldg(p.seq_lens + s.b) > p.max_blocks * p.block_size;
+    s.L = len[s.b] & ~kClampedBit;
+    s.clamped = (len[s.b] & kClampedBit) != 0;
     const int a = max(lo, pre[u]), z = min(hi, pre[u + 1]);
     s.t_lo = a - pre[u];
     s.t_hi = z - pre[u];
@@ -146,7 +150,8 @@ struct Sched {
 template <int R, bool FP8, int MT, bool PERSIST>
 __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
     decode_mma_kernel(const DecodeParams p,
-                      const __grid_constant__ CUtensorMap tmap) {
+                      const __grid_constant__ CUtensorMap tmap,
+                      const __grid_constant__ CUtensorMap qmap) {
   using C = MmaCfg<R, FP8, MT>;
   constexpr int D = C::D, NCH = C::NCH, NCW = C::NCW, STAGES = C::STAGES;
   constexpr int NT = R / 32;  // 8-column MMA tiles per warp in P.V
@@ -163,12 +168,21 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
   uint64_t* q_full = bar_empty + STAGES;
   uint64_t* q_empty = q_full + 2;
   int* pre = reinterpret_cast<int*>(smem + C::OFF_PRE);
+  int* lens = reinterpret_cast<int*>(smem + C::OFF_LEN);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = p.num_heads;
   const int nvec = p.rows_per_seq * H;
   const int qblocks = ceil_div(nvec, 16 * MT);
   const int S = p.num_splits;
+  if (threadIdx.x == NCW * 32) {
+    tma_prefetch_desc(&tmap);
+    if (p.q_tma) tma_prefetch_desc(&qmap);
+  }
+  // Launched overlapped with the previous kernel of the stream: nothing in
+  // global memory is read before it has completed.
+  griddep_wait();
+  griddep_launch_dependents();
 
   // ---------------------------------------------------------- schedule
   Sched sch;
@@ -177,8 +191,13 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
   if constexpr (PERSIST) {
     const int units = p.num_seqs * qblocks;
     // pre[u + 1] = tiles of unit u, then an inclusive scan by warp 0
-    for (int u = threadIdx.x; u < units; u += blockDim.x)
-      pre[u + 1] = ceil_div(clamp_len(p, u / qblocks), kBN);
+    for (int u = threadIdx.x; u < units; u += blockDim.x) {
+      const int b = u / qblocks;
+      const int raw = __ldg(p.seq_lens + b);
+      const int L = clamp_len(p, b);
+      pre[u + 1] = ceil_div(L, kBN);
+      if (u == b * qblocks) lens[b] = L | (raw > L ? kClampedBit : 0);
+    }
     if (threadIdx.x == 0) pre[0] = 0;
     __syncthreads();
     if (warp == 0) {
@@ -206,6 +225,7 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
     Cc = max(Cc, ceil_div(max_n, S - 1));  // at most S slots per unit
     Cc = max(Cc, 1);
     sch.pre = pre;
+    sch.len = lens;
     sch.units = units;
     sch.qblocks = qblocks;
     sch.C = Cc;
@@ -265,7 +285,8 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
       mbar_init(&bar_empty[i], NCW);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&q_full[i], 32);  // one cp.async arrival per producer lane
+      // TMA: one expect-tx arrival; cp.async: one arrival per producer lane
+      mbar_init(&q_full[i], p.q_tma ? 1 : 32);
       mbar_init(&q_empty[i], NCW);
     }
     fence_mbar_init();
@@ -293,7 +314,6 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
     const int rows_box = bs < kBN ? bs : kBN;
     const int npg = kBN / rows_box;
     constexpr int ROWB = FP8 ? 64 : 128;
-    if (lane == 0) tma_prefetch_desc(&tmap);
     int it = 0;  // tiles issued so far (ring position)
     for_each_seg([&](const Seg& sg, int k) -> bool {
       // Q of this segment -> buffer k & 1 (all lanes), once the consumers are
@@ -302,21 +322,41 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
         if (lane == 0 && p.err_count) atomicAdd(p.err_count, kTimeoutErr);
         return false;
       }
-      // cp.async: the copies proceed while this warp goes on issuing tiles;
-      // q_full completes when every lane's copies have landed.
-      const uint32_t s_q = smem_u32(smem + C::OFF_Q + (k & 1) * C::QBYTES);
       const int v0 = sg.g * 16 * MT;
-      for (int i = lane; i < 16 * MT * (D / 8); i += 32) {
-        const int qr = i / (D / 8), ch = i % (D / 8);
-        const int v = v0 + qr;
-        const uint16_t* src = p.q;
-        if (v < nvec) {
-          const int row = sg.b * p.rows_per_seq + v / H, h = v % H;
-          src = p.q + row * p.q_row_stride + h * p.q_head_stride + ch * 8;
+      uint8_t* q_dst = smem + C::OFF_Q + (k & 1) * C::QBYTES;
+      if (p.q_tma) {
+        // Heads come in multiples of 16, so each 16-vector M tile is 16
+        // consecutive heads of one row: one {64, 16, 1} box per 64 dims.
+        // M tiles past the last vector are not loaded (their rows stay
+        // unused).
+        if (lane == 0) {
+          int ntile = 0;
+          for (int i = 0; i < MT; ++i) ntile += v0 + 16 * i < nvec ? 1 : 0;
+          mbar_arrive_expect_tx(&q_full[k & 1], static_cast<uint32_t>(ntile * NCH * 2048));
+          for (int i = 0; i < ntile; ++i) {
+            const int v = v0 + 16 * i;
+            const int row = sg.b * p.rows_per_seq + v / H, h0 = v % H;
+            for (int c = 0; c < NCH; ++c)
+              tma_load_3d(q_dst + c * C::QBOX + i * 2048, &qmap, &q_full[k & 1], c * 64, h0,
+                          row);
+          }
         }
-        cp_async16(s_q + (ch >> 3) * C::QBOX + sw128(qr, ch & 7), src, v < nvec ? 16u : 0u);
+      } else {
+        // cp.async: the copies proceed while this warp goes on issuing
+        // tiles; q_full completes when every lane's copies have landed.
+        const uint32_t s_q = smem_u32(q_dst);
+        for (int i = lane; i < 16 * MT * (D / 8); i += 32) {
+          const int qr = i / (D / 8), ch = i % (D / 8);
+          const int v = v0 + qr;
+          const uint16_t* src = p.q;
+          if (v < nvec) {
+            const int row = sg.b * p.rows_per_seq + v / H, h = v % H;
+            src = p.q + row * p.q_row_stride + h * p.q_head_stride + ch * 8;
+          }
+          cp_async16(s_q + (ch >> 3) * C::QBOX + sw128(qr, ch & 7), src, v < nvec ? 16u : 0u);
+        }
+        cp_async_arrive(&q_full[k & 1]);
       }
-      cp_async_arrive(&q_full[k & 1]);
       if (lane == 0) {
         const int32_t* bt = p.block_table + static_cast<int64_t>(sg.b) * p.bt_stride;
         // block ids of the next tile are loaded one tile ahead
@@ -616,8 +656,8 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
 }
 
 template <int R, bool FP8, int MT, bool PERSIST>
-cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmap, int sm_count,
-                      cudaStream_t stream) {
+cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmap, const CUtensorMap& qmap,
+                      int sm_count, cudaStream_t stream) {
   using C = MmaCfg<R, FP8, MT>;
   static bool attr_done = false;  // per instantiation; benign race
   if (!attr_done) {
@@ -629,41 +669,38 @@ cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmap, int sm_cou
   }
   const int nvec = p.rows_per_seq * p.num_heads;
   const int qblocks = (nvec + 16 * MT - 1) / (16 * MT);
-  if constexpr (PERSIST) {
-    decode_mma_kernel<R, FP8, MT, true><<<sm_count, C::NTHREADS, C::SMEM, stream>>>(p, tmap);
-  } else {
-    const dim3 grid(qblocks, p.num_splits, p.num_seqs);
-    decode_mma_kernel<R, FP8, MT, false><<<grid, C::NTHREADS, C::SMEM, stream>>>(p, tmap);
-  }
-  return cudaGetLastError();
+  const dim3 grid = PERSIST ? dim3(sm_count) : dim3(qblocks, p.num_splits, p.num_seqs);
+  return launch_overlapped(decode_mma_kernel<R, FP8, MT, PERSIST>, grid, dim3(C::NTHREADS),
+                           C::SMEM, stream, p, tmap, qmap);
 }
 
 template <int R, bool FP8, int MT>
-cudaError_t launch_r2(const DecodeParams& p, const CUtensorMap& tmap, int sm_count,
-                      cudaStream_t stream) {
+cudaError_t launch_r2(const DecodeParams& p, const CUtensorMap& tmap, const CUtensorMap& qmap,
+                      int sm_count, cudaStream_t stream) {
   const int qblocks = (p.rows_per_seq * p.num_heads + 16 * MT - 1) / (16 * MT);
   const int64_t units = static_cast<int64_t>(qblocks) * p.num_seqs;
   if (p.num_splits > 1 && units <= kMaxPersistUnits)
-    return launch_mt<R, FP8, MT, true>(p, tmap, sm_count, stream);
-  return launch_mt<R, FP8, MT, false>(p, tmap, sm_count, stream);
+    return launch_mt<R, FP8, MT, true>(p, tmap, qmap, sm_count, stream);
+  return launch_mt<R, FP8, MT, false>(p, tmap, qmap, sm_count, stream);
 }
 
 template <int R, bool FP8>
-cudaError_t launch_r(const DecodeParams& p, const CUtensorMap& tmap, int sm_count,
-                     cudaStream_t stream) {
+cudaError_t launch_r(const DecodeParams& p, const CUtensorMap& tmap, const CUtensorMap& qmap,
+                     int sm_count, cudaStream_t stream) {
   const int nvec = p.rows_per_seq * p.num_heads;
-  if (nvec <= 16) return launch_r2<R, FP8, 1>(p, tmap, sm_count, stream);
-  return launch_r2<R, FP8, 2>(p, tmap, sm_count, stream);
+  if (nvec <= 16) return launch_r2<R, FP8, 1>(p, tmap, qmap, sm_count, stream);
+  return launch_r2<R, FP8, 2>(p, tmap, qmap, sm_count, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap,
-                              int R, bool fp8, int sm_count, cudaStream_t stream) {
-  if (R == 512) return fp8 ? launch_r<512, true>(p, tmap, sm_count, stream)
-                           : launch_r<512, false>(p, tmap, sm_count, stream);
-  return fp8 ? launch_r<256, true>(p, tmap, sm_count, stream)
-             : launch_r<256, false>(p, tmap, sm_count, stream);
+                              const CUtensorMap& qmap, int R, bool fp8, int sm_count,
+                              cudaStream_t stream) {
+  if (R == 512) return fp8 ? launch_r<512, true>(p, tmap, qmap, sm_count, stream)
+                           : launch_r<512, false>(p, tmap, qmap, sm_count, stream);
+  return fp8 ? launch_r<256, true>(p, tmap, qmap, sm_count, stream)
+             : launch_r<256, false>(p, tmap, qmap, sm_count, stream);
 }
 
 }  // namespace mla

@@ -112,6 +112,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   const int nvec = p.rows_per_seq * H;
   const int v0 = g_blk * 128;
   const int S = p.num_splits;
+  if (threadIdx.x == 128) tma_prefetch_desc(&tmap);
+  // Launched overlapped with the previous kernel of the stream: nothing in
+  // global memory is read before it has completed.
+  griddep_wait();
+  griddep_launch_dependents();
 
   int L = __ldg(p.seq_lens + b);
   const int Lmax = p.max_blocks * p.block_size;
@@ -206,7 +211,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmap);
       const int bs = p.block_size;
       const int rows_box = bs < TBN ? bs : TBN;
       const int npg = TBN / rows_box;
@@ -509,8 +513,8 @@ cudaError_t launch_decode_tc(const DecodeParams& p, const CUtensorMap& tmap,
   const int qblocks = (p.rows_per_seq * p.num_heads + 127) / 128;
   const int groups = (p.num_splits + split_group - 1) / split_group;
   const dim3 grid(2 * qblocks, groups, p.num_seqs);
-  decode_tc_kernel<<<grid, TC_THREADS, TC_SMEM, stream>>>(p, tmap, split_group);
-  return cudaGetLastError();
+  return launch_overlapped(decode_tc_kernel, grid, dim3(TC_THREADS), TC_SMEM, stream, p, tmap,
+                           split_group);
 }
 
 }  // namespace mla

@@ -30,7 +30,27 @@ struct DecodeParams {
   uint16_t* o;    // bf16 [rows, H, R]
   float* lse;     // fp32 [rows, H]
   int* err_count;
+  int q_tma;      // the warp-MMA kernel loads Q through its q tensor map
 };
+
+// Launches `kernel` so that it may start while the previous kernel of the
+// stream is still running (programmatic stream serialization).  Every kernel
+// launched this way calls griddep_wait() before touching global memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                                     size_t smem, cudaStream_t stream, const Args&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 cudaError_t launch_cache_write(const void* kv_c, int64_t kv_c_stride,
                                const void* k_pe, int64_t k_pe_stride,
@@ -43,9 +63,14 @@ cudaError_t launch_cache_write(const void* kv_c, int64_t kv_c_stride,
 // Stage 1 on warp-level MMA (mma.sync m16n8k16), any head count.  `tmap` is
 // a 3-D tiled tensor map over the cache {R+P, block_size, num_blocks} with a
 // {64, min(block_size, 64), 1} box: 128-byte swizzle for bf16, none for fp8.
-// With num_kv_splits > 1 it runs persistent, one CTA per SM (`sm_count`).
+// With p.q_tma, `qmap` is a 3-D map over q {R+P, H, rows} with a {64, 16, 1}
+// box and 128-byte swizzle (heads a multiple of 16); otherwise it is unused
+// and Q is gathered with cp.async.  With num_kv_splits > 1 it runs
+// persistent, one CTA per SM (`sm_count`).  Launched overlapped with the
+// previous kernel of the stream.
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap,
-                              int R, bool fp8, int sm_count, cudaStream_t stream);
+                              const CUtensorMap& qmap, int R, bool fp8, int sm_count,
+                              cudaStream_t stream);
 
 // Stage 1 on tcgen05/TMEM for bf16 caches with R = 512: one 2-CTA cluster per
 // 128 query vectors and group of `split_group` consecutive splits.  `tmap` as

@@ -10,6 +10,9 @@
 //
 // One warp per (row, head); each lane owns R/32 latent columns in 16-byte
 // groups, so every partial row is read with coalesced 512-byte warp loads.
+// The split weights are computed from all lse values first, so the partial
+// rows of several splits are in flight at once instead of one round trip per
+// split.
 // Stage 1 leaves every split slot of a non-empty sequence either holding a
 // partial or marked with lse = -inf (a slot its partition did not use); the
 // merge visits the slots in index order and skips the marked ones, so it
@@ -30,6 +33,7 @@ template <int R>
 __global__ void __launch_bounds__(kMergeWarps * 32)
     merge_kernel(const DecodeParams p) {
   constexpr int NV = R / 128;  // float4 groups per lane
+  griddep_wait();              // stage 1's partials are complete and visible
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   const int H = p.num_heads;
@@ -56,23 +60,47 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   float4 acc[NV];
 #pragma unroll
   for (int k = 0; k < NV; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
-  for (int s = 0; s < S; ++s) {
-    const int64_t rec = rec0 + static_cast<int64_t>(s) * H;
-    const float ls = p.ws_lse[rec];
-    if (ls == -INFINITY) continue;  // a slot stage 1 left without a partial
-    const float w = __expf(ls - M);
-    const float4* src = reinterpret_cast<const float4*>(p.ws_o + rec * R);
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-      const float4 v = src[k * 32 + lane];
-      acc[k].x += w * v.x;
-      acc[k].y += w * v.y;
-      acc[k].z += w * v.z;
-      acc[k].w += w * v.w;
-    }
+  float den = 0.f;  // this lane's slots; summed over the warp at the end
+  for (int c = 0; c < S; c += 32) {
+    // Lane j holds the weight of slot c + j; the partial rows of up to four
+    // non-empty slots are loaded together, then added in slot order.
+    const int s = c + lane;
+    const float ls = s < S ? p.ws_lse[rec0 + static_cast<int64_t>(s) * H] : -INFINITY;
+    const float w = ls == -INFINITY ? 0.f : __expf(ls - M);
     den += w;
+    uint32_t mask = __ballot_sync(0xffffffffu, w != 0.f);
+    while (mask) {
+      int js[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        js[u] = mask ? __ffs(mask) - 1 : -1;
+        mask &= mask ? mask - 1 : 0u;
+      }
+      float4 v[4][NV];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (js[u] < 0) continue;
+        const float4* src = reinterpret_cast<const float4*>(
+            p.ws_o + (rec0 + static_cast<int64_t>(c + js[u]) * H) * R);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) v[u][k] = src[k * 32 + lane];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (js[u] < 0) continue;
+        const float wj = __shfl_sync(0xffffffffu, w, js[u]);
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+          acc[k].x += wj * v[u][k].x;
+          acc[k].y += wj * v[u][k].y;
+          acc[k].z += wj * v[u][k].z;
+          acc[k].w += wj * v[u][k].w;
+        }
+      }
+    }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
   const float inv = 1.f / den;
 #pragma unroll
   for (int k = 0; k < NV; ++k)
@@ -88,11 +116,11 @@ cudaError_t launch_merge(const DecodeParams& p, int R, cudaStream_t stream) {
   const int64_t pairs = static_cast<int64_t>(p.num_rows) * p.num_heads;
   if (pairs == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>((pairs + kMergeWarps - 1) / kMergeWarps));
-  if (R == 512)
-    merge_kernel<512><<<grid, kMergeWarps * 32, 0, stream>>>(p);
-  else
-    merge_kernel<256><<<grid, kMergeWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  // Overlaps its launch with the tail of stage 1 (which lets it start early).
+  return R == 512 ? launch_overlapped(merge_kernel<512>, grid, dim3(kMergeWarps * 32), 0,
+                                      stream, p)
+                  : launch_overlapped(merge_kernel<256>, grid, dim3(kMergeWarps * 32), 0,
+                                      stream, p);
 }
 
 }  // namespace mla

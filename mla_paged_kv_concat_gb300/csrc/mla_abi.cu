@@ -79,6 +79,26 @@ mla_status make_cache_tmap(CUtensorMap* map, const void* cache, bool fp8,
   return MLA_OK;
 }
 
+// Tensor map over q viewed as {R+P (dims), H, rows}: one box is 64 dims of
+// 16 consecutive heads of one row, 128-byte swizzled (the layout of the
+// warp-MMA kernel's Q buffer).  Needs 16-byte strides (validated) and heads a
+// multiple of 16; returns false when q does not qualify.
+bool make_q_tmap(CUtensorMap* map, const void* q, int D, int H, int rows,
+                 int64_t q_head_stride, int64_t q_row_stride) {
+  auto fn = encode_fn();
+  if (!fn || H % 16 != 0) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(q_head_stride) * 2,
+                           static_cast<cuuint64_t>(q_row_stride) * 2};
+  cuuint32_t box[3] = {64, 16, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool supported_latent(int R, int P) {
   return (R == 512 || R == 256) && P == 64;
 }
@@ -252,6 +272,7 @@ mla_status prepare_decode(const void* q, int64_t q_row_stride,
   p->o = static_cast<uint16_t*>(o);
   p->lse = lse;
   p->err_count = err_count;
+  p->q_tma = 0;
   return MLA_OK;
 }
 
@@ -265,18 +286,25 @@ bool use_tc(const mla::DecodeParams& p, bool fp8, int R, mla_decode_path path) {
          static_cast<int64_t>(p.rows_per_seq) * p.num_heads >= 128;
 }
 
-mla_status run_stage1(const mla::DecodeParams& p, const void* kv_cache,
+mla_status run_stage1(const mla::DecodeParams& p_in, const void* kv_cache,
                       bool fp8, int R, int block_size, int num_blocks,
                       int64_t block_stride, mla_decode_path path,
                       cudaStream_t s) {
-  CUtensorMap tmap;
+  mla::DecodeParams p = p_in;
+  CUtensorMap tmap, qmap;
   const bool tc = use_tc(p, fp8, R, path);
   mla_status st = make_cache_tmap(&tmap, kv_cache, fp8, R + 64, block_size,
                                   num_blocks, block_stride, 64);
   if (st != MLA_OK) return st;
+  memset(&qmap, 0, sizeof qmap);
+  if (!tc)
+    p.q_tma = make_q_tmap(&qmap, p.q, R + 64, p.num_heads, p.num_rows, p.q_head_stride,
+                          p.q_row_stride)
+                  ? 1
+                  : 0;
   cudaError_t e =
       tc ? mla::launch_decode_tc(p, tmap, mla::tc_split_group(p, device_sm_count()), s)
-         : mla::launch_decode_mma(p, tmap, R, fp8, device_sm_count(), s);
+         : mla::launch_decode_mma(p, tmap, qmap, R, fp8, device_sm_count(), s);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 

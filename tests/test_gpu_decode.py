@@ -161,6 +161,28 @@ def test_padded_block_stride(cuda_dev):
     assert_close(o, lse, o_ref, lse_ref, what="padded stride")
 
 
+@pytest.mark.parametrize("H,path", [(16, mla.MLA_PATH_MMA_SYNC), (32, mla.MLA_PATH_MMA_SYNC),
+                                    (8, mla.MLA_PATH_MMA_SYNC), (128, mla.MLA_PATH_TCGEN05)])
+def test_strided_q(cuda_dev, H, path):
+    """q as a view with padded heads and padded rows (head stride 640, row
+    stride (H + 2) * 640 elements): the tensor-map and the gathered Q loads
+    must both follow the strides."""
+    w = W.make_workload("qstride", seed=65, seq_lens=[190, 64, 301], num_heads=H)
+    d = Dev(w)
+    d.write()
+    rows, D = w.num_rows, w.head_dim
+    big = torch.full((rows, H + 2, 640), float("nan"), dtype=torch.bfloat16, device="cuda")
+    big[:, :H, :D] = d.q
+    q_view = big[:, :H, :D]
+    assert q_view.stride(1) == 640 and q_view.stride(0) == (H + 2) * 640
+    for splits in (1, 3):
+        o, lse = mla.decode(q_view, d.cache, d.block_table, d.seq_lens, w.sm_scale, splits,
+                            path=path)
+        torch.cuda.synchronize()
+        o_ref, lse_ref = oracle_decode(w, oracle_cache(w))
+        assert_close(o, lse, o_ref, lse_ref, what=f"strided q H={H} S={splits}")
+
+
 def test_split_count_does_not_change_result_beyond_rounding(cuda_dev):
     w = W.make("per_shard")
     d = Dev(w)
