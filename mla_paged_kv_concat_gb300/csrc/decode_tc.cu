@@ -14,27 +14,33 @@
 // the latent dimension is split over a 2-CTA cluster:
 //   rank 0 holds dims [0, 256)   : S partial over them, O[:, 0:256)
 //   rank 1 holds dims [256, 576) : S partial over them, O[:, 256:512)
-// Each CTA loads only its own dims of every KV tile (no byte is read twice),
-// computes its partial S into TMEM, and the two partials are exchanged
-// through distributed shared memory (st.async completing on the peer's
-// mbarrier); both CTAs then run the same softmax on S = S_lo + S_hi
-// (identical bits on both sides) and each accumulates its half of O.
+// Each CTA loads only its own dims of every KV tile (no byte is read twice)
+// and computes its partial S into TMEM.  The softmax of vector v is owned by
+// one CTA (rank v / 64): the other CTA sends it its partial S row for v
+// (fp32, one bulk shared-memory copy per tile for 64 vectors), the owner adds
+// the two partials, runs the online softmax and sends P (bf16) back with the
+// row's rescale factor; both CTAs then accumulate their half of O with P as
+// the A operand.  Per tile and direction that is 16 KiB of scores plus 8 KiB
+// of P, and each CTA evaluates only 64 x 64 exponentials.
 //
 // TMEM (512 columns): O [0, 256), S [256, 320), P [320, 352) as packed
 // bf16, Q [352, 512) as packed bf16 (rank 1 needs 160 columns for its 320
 // dims).  Q and P are A operands read straight from TMEM by the MMAs; only K
-// and V tiles live in shared memory, which leaves room for a 4-stage ring of
-// 64-token tiles (enough bytes in flight to cover the HBM latency).  Tiles
-// are 64 tokens so that each S MMA has N = 64 (an MMA instruction costs
-// about the same to issue up to N = 64).
+// and V tiles and the exchange buffers live in shared memory.  The ring is
+// short (4 stages of 64 tokens), so the producer also prefetches the tiles
+// a few steps ahead into L2.
 //
-// Roles per CTA (192 threads):
-//   warps 0-3  softmax: thread i owns TMEM lane i = query vector i; the
-//              row max / row sum are thread-local; lazy rescaling of O
-//              (only when the running max grows by more than 2^8);
-//   warp 4     TMA producer: 64-token tiles of the paged cache into a
+// Roles per CTA (256 threads):
+//   warps 0-3  softmax: thread i owns TMEM lane i = query vector i.  The two
+//              warps of the vectors this CTA owns run the softmax (row max
+//              and sum thread-local, lazy rescaling of O only when the
+//              running max grows by more than 2^8); the other two forward
+//              their rows' partial scores and store the P they get back;
+//   one warp   MMA issuer (one thread) and TMEM owner;
+//   one warp   TMA producer: 64-token tiles of the paged cache into a
 //              4-stage mbarrier ring (128-byte swizzled boxes);
-//   warp 5     MMA issuer (one thread) and TMEM owner.
+//   the MMA and producer warps sit on the sub-partitions of the forwarding
+//   warps (the two remaining warps only join the final barrier).
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -48,18 +54,24 @@ namespace {
 
 constexpr int TBN = 64;                   // tokens per tile
 constexpr int TSTAGES = 4;                // KV ring depth
+constexpr int TPREFETCH = 4;              // tiles fetched into L2 ahead of the ring
 constexpr int TMAXCH = 5;                 // max 64-dim chunks per CTA
 constexpr int CHUNK_BYTES = TBN * 128;    // one 64-dim box of a tile (8 KiB)
 constexpr int STAGE_BYTES = TMAXCH * CHUNK_BYTES;
-constexpr int XS_ROW = TBN * 4;           // bytes of one exchanged S row
-constexpr int XS_BYTES = 128 * XS_ROW;
+constexpr int XS_ROW = TBN * 4;           // bytes of one partial-score row
+constexpr int XS_BYTES = 64 * XS_ROW;     // 64 vectors' partial scores
+constexpr int XP_ROW = TBN * 2;           // bytes of one P row (bf16)
+constexpr int XP_ALPHA = 64 * XP_ROW;     // offset of the 64 per-row factors
+constexpr int XP_BYTES = XP_ALPHA + 64 * 4;
 constexpr int OFF_STAGE = 0;
-constexpr int OFF_XS = OFF_STAGE + TSTAGES * STAGE_BYTES;
-constexpr int OFF_BAR = OFF_XS + 2 * XS_BYTES;
-constexpr int NBARS = 2 * TSTAGES + 2 + 4 + 1;
+constexpr int OFF_XIN = OFF_STAGE + TSTAGES * STAGE_BYTES;  // peer partials, x2
+constexpr int OFF_PIN = OFF_XIN + 2 * XS_BYTES;             // P from the peer, x2
+constexpr int OFF_FIN = OFF_PIN + 2 * XP_BYTES;             // 1 / l from the peer
+constexpr int OFF_BAR = OFF_FIN + 256;
+constexpr int NBARS = 2 * TSTAGES + 5 + 5;
 constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
 constexpr int TC_SMEM = OFF_TMEMSLOT + 16 + 1024;  // + alignment slack
-constexpr int TC_THREADS = 192;
+constexpr int TC_THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t S_COL = 256;  // S, 64 fp32 columns
 constexpr uint32_t P_COL = 320;  // P, 64 bf16 in 32 columns
@@ -68,7 +80,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-static_assert(OFF_XS % 1024 == 0, "alignment");
+static_assert(OFF_XIN % 1024 == 0 && XS_BYTES % 16 == 0 && XP_BYTES % 16 == 0,
+              "alignment");
 static_assert(TC_SMEM <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -78,11 +91,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   const bool ok = mbar_wait(bar, parity);
   return __all_sync(0xffffffffu, ok);
 }
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity) {
+  const bool ok = tc::mbar_wait_cluster(bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
 
-// Byte offset of 16-byte chunk `c` (0..15) of exchanged S row `r`: the chunk
-// index is XORed with r mod 8 so that 8 consecutive rows hit all 32 banks.
-__device__ __forceinline__ uint32_t xs_off(uint32_t r, uint32_t c) {
-  return r * XS_ROW + ((c ^ (r & 7u)) << 4);
+// Byte offset of 16-byte chunk `c` of row `r` in an exchange buffer whose
+// rows are `row_bytes` long: the chunk index is XORed with r mod 8 so that
+// eight consecutive rows hit all 32 banks.
+__device__ __forceinline__ uint32_t xoff(uint32_t r, uint32_t c, uint32_t row_bytes) {
+  return r * row_bytes + ((c ^ (r & 7u)) << 4);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
@@ -94,12 +112,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + TSTAGES;
-  uint64_t* xs_full = bars + 2 * TSTAGES;  // two exchange buffers
-  uint64_t* s_full = xs_full + 2;
-  uint64_t* s_free = xs_full + 3;
-  uint64_t* p_full = xs_full + 4;
-  uint64_t* pv_done = xs_full + 5;
-  uint64_t* mma_done = xs_full + 6;
+  uint64_t* s_full = bars + 2 * TSTAGES;
+  uint64_t* s_free = s_full + 1;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* pv_done = s_full + 3;
+  uint64_t* mma_done = s_full + 4;
+  uint64_t* xin_full = s_full + 5;   // [2] peer partial scores landed
+  uint64_t* pin_full = s_full + 7;   // [2] peer P landed
+  uint64_t* fin_full = s_full + 9;   // peer's 1 / l landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEMSLOT);
 
   const uint32_t rank = tc::cluster_ctarank();
@@ -107,6 +127,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   const int nch = rank == 0 ? 4 : 5;       // local 64-dim chunks
   const int c0 = rank == 0 ? 0 : 4;        // first global chunk
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The MMA issuer and the producer share the SM sub-partitions (warp % 4)
+  // of the two softmax warps that only forward rows, not of the two that run
+  // the softmax: warps 2, 3 forward on rank 0, warps 0, 1 on rank 1.
+  const int mma_warp = rank == 0 ? 6 : 4;
+  const int prod_warp = mma_warp + 1;
   const int g_blk = blockIdx.x >> 1, ysplit = blockIdx.y, b = blockIdx.z;
   const int H = p.num_heads;
   const int nvec = p.rows_per_seq * H;
@@ -161,15 +186,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(&xs_full[i], 1);  // expect_tx by one thread
     mbar_init(s_full, 1);
     mbar_init(s_free, 128);
     mbar_init(p_full, 128);
     mbar_init(pv_done, 1);
     mbar_init(mma_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&xin_full[i], 1);  // local expect-tx arrival + the peer's bytes
+      mbar_init(&pin_full[i], 1);
+    }
+    mbar_init(fin_full, 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == mma_warp) {
     tc::tmem_alloc(tmem_slot, TMEM_COLS);
     tc::tmem_relinquish();
   }
@@ -208,30 +237,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   tc::fence_after_sync();
   const uint32_t stage_base = smem_u32(smem + OFF_STAGE);
 
-  if (warp == 4) {
+  if (warp == prod_warp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const int bs = p.block_size;
       const int rows_box = bs < TBN ? bs : TBN;
       const int npg = TBN / rows_box;
       const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+      // Block ids of tile t (pages past the split end read as 0; they are
+      // neither loaded nor prefetched).
+      auto ids_of = [&](int t, int (&ids)[4]) {
+#pragma unroll
+        for (int pg = 0; pg < 4; ++pg) {
+          const int tk = start + t * TBN + pg * rows_box;
+          ids[pg] = (pg < npg && t < ntiles && tk < end) ? __ldg(bt + tk / bs) : 0;
+        }
+      };
+      auto pages_of = [&](int t) {
+        int n = 0;
+        for (int pg = 0; pg < npg; ++pg)
+          if (start + t * TBN + pg * rows_box < end) ++n;
+        return t < ntiles ? n : 0;
+      };
+      auto prefetch = [&](const int (&ids)[4], int t) {
+        const int np = pages_of(t);
+#pragma unroll
+        for (int pg = 0; pg < 4; ++pg) {
+          if (pg >= np) break;
+          if (ids[pg] < 0 || ids[pg] >= p.num_blocks) continue;
+          const int row0 = (start + t * TBN + pg * rows_box) % bs;
+          for (int cl = 0; cl < nch; ++cl)
+            tma_prefetch_l2_3d(&tmap, (c0 + cl) * 64, row0, ids[pg]);
+        }
+      };
+      // Ids are read one tile before they are used, so the block-table
+      // latency hides behind a tile's worth of waiting.
+      int cur[4], nxt[4], pf[4], first[TPREFETCH][4];
+      ids_of(0, cur);
+#pragma unroll
+      for (int t = 0; t < TPREFETCH; ++t) ids_of(t + 1, first[t]);
+      ids_of(TPREFETCH + 1, pf);
       for (int n = 0; n < ntiles; ++n) {
+        ids_of(n + 1, nxt);
         const int st = n % TSTAGES;
         const uint32_t ph = (n / TSTAGES) & 1;
         if (!mbar_wait(&kv_empty[st], ph ^ 1)) {
           if (p.err_count) atomicAdd(p.err_count, kTimeoutErr);
           break;
         }
-        const int tok0 = start + n * TBN;
-        int npages = 0;
-        for (int pg = 0; pg < npg; ++pg)
-          if (tok0 + pg * rows_box < end) ++npages;
+        const int npages = pages_of(n);
         mbar_arrive_expect_tx(&kv_full[st],
                               static_cast<uint32_t>(npages * nch * rows_box * 128));
         uint8_t* dst = smem + OFF_STAGE + st * STAGE_BYTES;
-        for (int pg = 0; pg < npages; ++pg) {
-          const int t = tok0 + pg * rows_box;
-          const int blk = __ldg(bt + t / bs);
+#pragma unroll
+        for (int pg = 0; pg < 4; ++pg) {
+          if (pg >= npages) break;
+          const int t = start + n * TBN + pg * rows_box;
+          const int blk = cur[pg];
           const int row0 = t % bs;
           if ((blk < 0 || blk >= p.num_blocks) && p.err_count && rank == 0)
             atomicAdd(p.err_count, 1);
@@ -239,176 +301,313 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             tma_load_3d(dst + cl * CHUNK_BYTES + pg * rows_box * 128, &tmap,
                         &kv_full[st], (c0 + cl) * 64, row0, blk);
         }
+        if (n == 0) {
+          // tiles 1 .. TPREFETCH, once the first tile's loads are on their way
+#pragma unroll
+          for (int t = 0; t < TPREFETCH; ++t) prefetch(first[t], t + 1);
+        }
+        // L2 prefetch of tile n + 1 + TPREFETCH (ids read one tile ago)
+        prefetch(pf, n + 1 + TPREFETCH);
+        ids_of(n + 2 + TPREFETCH, pf);
+#pragma unroll
+        for (int pg = 0; pg < 4; ++pg) cur[pg] = nxt[pg];
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == mma_warp) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idS = tc::idesc_bf16(128, TBN, 0, 0);
     constexpr uint32_t idPV = tc::idesc_bf16(128, 256, 0, 1);
-    const int nks = nch * 4;
+    // S of tile n needs its KV stage and the S columns (every softmax thread
+    // has read S of tile n - 1); P.V of tile k needs P of tile k.  The two
+    // streams are issued as soon as each is ready, so S runs ahead of the
+    // P round trip between the CTAs.
+    int ns = 0, npv = 0;
     bool ok = true;
-    auto issue_pv = [&](int k) -> bool {
-      if (!warp_wait(p_full, k & 1)) return false;
-      tc::fence_after_sync();
-      if (lane == 0) {
-        const uint32_t stb = stage_base + (k % TSTAGES) * STAGE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < TBN / 16; ++kk) {
+    uint64_t t_idle = 0;
+    uint32_t spins = 0;
+    while (npv < ntiles) {
+      bool progress = false;
+      // P.V first: it releases a KV stage and the P columns.  (Lane 0
+      // decides, so the warp stays converged.)
+      const bool pv_ready = __shfl_sync(0xffffffffu, npv < ns && mbar_test(p_full, npv & 1), 0);
+      if (pv_ready) {
+        tc::fence_after_sync();
+        if (lane == 0) {
           // A = P (TMEM, 16 tokens = 8 packed columns per step); B = V:
-          // MN-major, 128-byte swizzle (N step = next 64-dim box, K step =
-          // 8 tokens = 1024 B).
-          const uint64_t bd = tc::smem_desc(stb + kk * 2048, CHUNK_BYTES, 1024,
-                                            tc::kLayoutSw128);
-          tc::mma_ts(tmem, tmem + P_COL + kk * 8, bd, idPV, (k > 0 || kk > 0) ? 1u : 0u);
+          // MN-major, 128-byte swizzle (N step = next 64-dim box, K step = 8
+          // tokens = 1024 B; 16 tokens per MMA = 2048 B = 128 in the field).
+          const uint64_t d0 = tc::smem_desc(stage_base + (npv % TSTAGES) * STAGE_BYTES,
+                                            CHUNK_BYTES, 1024, tc::kLayoutSw128);
+#pragma unroll
+          for (int kk = 0; kk < TBN / 16; ++kk)
+            tc::mma_ts(tmem, tmem + P_COL + kk * 8, d0 + static_cast<uint64_t>(kk * 128), idPV,
+                       (npv > 0 || kk > 0) ? 1u : 0u);
+          tc::commit(pv_done);
+          tc::commit(&kv_empty[npv % TSTAGES]);
         }
-        tc::commit(pv_done);
-        tc::commit(&kv_empty[k % TSTAGES]);
-      }
-      __syncwarp();
-      return true;
-    };
-    for (int n = 0; n < ntiles && ok; ++n) {
-      const int st = n % TSTAGES;
-      if (!warp_wait(&kv_full[st], (n / TSTAGES) & 1)) {
-        ok = false;
-        break;
-      }
-      const int valid = min(TBN, end - (start + n * TBN));
-      if (valid < TBN) {
-        // Rows past the split end hold other tokens or NaN: zero them so the
-        // P.V product sees 0 * 0 there (their scores are masked to -inf).
-        uint8_t* stp = smem + OFF_STAGE + st * STAGE_BYTES;
-        const int nz = (TBN - valid) * nch * 8;
-        for (int i = lane; i < nz; i += 32) {
-          const int r = valid + i / (nch * 8), rem = i % (nch * 8);
-          *reinterpret_cast<uint4*>(stp + (rem >> 3) * CHUNK_BYTES + r * 128 +
-                                    (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
         __syncwarp();
+        ++npv;
+        progress = true;
       }
-      if (n >= 1 && !warp_wait(s_free, (n - 1) & 1)) {
-        ok = false;
-        break;
-      }
-      tc::fence_after_sync();
-      if (lane == 0) {
-        // S = Q K^T: A = Q from TMEM (16 dims = 8 packed columns per step),
-        // B = K tile, K-major with 128-byte swizzle.
-        const uint32_t stb = stage_base + st * STAGE_BYTES;
-        for (int ks = 0; ks < nks; ++ks) {
-          const uint64_t bd = tc::smem_desc(stb + (ks >> 2) * CHUNK_BYTES + (ks & 3) * 32, 16,
-                                            1024, tc::kLayoutSw128);
-          tc::mma_ts(tmem + S_COL, tmem + Q_COL + ks * 8, bd, idS, ks > 0 ? 1u : 0u);
+      const bool s_ready = __shfl_sync(
+          0xffffffffu,
+          ns < ntiles && mbar_test(&kv_full[ns % TSTAGES], (ns / TSTAGES) & 1) &&
+              (ns == 0 || mbar_test(s_free, (ns - 1) & 1)),
+          0);
+      if (s_ready) {
+        const int st = ns % TSTAGES;
+        const int valid = min(TBN, end - (start + ns * TBN));
+        if (valid < TBN) {
+          // Rows past the split end hold other tokens or NaN: zero them so
+          // the P.V product sees 0 * 0 there (their scores are masked).
+          uint8_t* stp = smem + OFF_STAGE + st * STAGE_BYTES;
+          const int nz = (TBN - valid) * nch * 8;
+          for (int i = lane; i < nz; i += 32) {
+            const int r = valid + i / (nch * 8), rem = i % (nch * 8);
+            *reinterpret_cast<uint4*>(stp + (rem >> 3) * CHUNK_BYTES + r * 128 +
+                                      (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
         }
-        tc::commit(s_full);
+        tc::fence_after_sync();
+        if (lane == 0) {
+          // S = Q K^T: A = Q from TMEM (16 dims = 8 packed columns per
+          // step), B = K tile, K-major with 128-byte swizzle.  The
+          // descriptor's start-address field (bytes / 16) is advanced by
+          // addition: one 64-dim box is CHUNK_BYTES / 16, one 16-dim step 2.
+          const uint64_t d0 =
+              tc::smem_desc(stage_base + st * STAGE_BYTES, 16, 1024, tc::kLayoutSw128);
+#pragma unroll 1
+          for (int c = 0; c < nch; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const int ks = c * 4 + kk;
+              tc::mma_ts(tmem + S_COL, tmem + Q_COL + ks * 8,
+                         d0 + static_cast<uint64_t>(c * (CHUNK_BYTES >> 4) + kk * 2), idS,
+                         ks > 0 ? 1u : 0u);
+            }
+          }
+          tc::commit(s_full);
+        }
+        __syncwarp();
+        ++ns;
+        progress = true;
       }
-      __syncwarp();
-      if (n >= 1 && !issue_pv(n - 1)) {
-        ok = false;
-        break;
+      if (progress) {
+        t_idle = 0;
+        spins = 0;
+      } else if ((++spins & 1023u) == 0) {
+        // bounded: give up when nothing became ready for the wait limit
+        // (the timer is read every 1024 idle polls; it is slow to read)
+        const uint64_t now = globaltimer();
+        if (t_idle == 0) {
+          t_idle = now;
+        } else if (now - t_idle > kWaitTimeoutNs) {
+          ok = false;
+          break;
+        }
       }
     }
-    if (ok) ok = issue_pv(ntiles - 1);
     if (!ok && lane == 0 && p.err_count) atomicAdd(p.err_count, kTimeoutErr);
     if (lane == 0) tc::commit(mma_done);
     __syncwarp();
     warp_wait(mma_done, 0);  // nothing of ours still runs on the tensor core
-  } else {
+  } else if (warp < 4) {
     // ------------------------------------------------------------ softmax
     const int row_i = threadIdx.x;  // TMEM lane / query vector
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const bool own = static_cast<uint32_t>(row_i >> 6) == rank;  // this CTA's softmax rows
+    const int xi = row_i & 63;      // row within the 64-vector exchange blocks
+    const bool lead = xi == 0;      // registers the expected bytes of each message
     const float scale_log2 = p.sm_scale * kLog2e;
-    const uint32_t xs_local = smem_u32(smem + OFF_XS);
-    const uint32_t xs_peer = tc::map_peer(xs_local, peer);
-    const uint32_t xsbar_peer0 = tc::map_peer(smem_u32(&xs_full[0]), peer);
-    const uint32_t xsbar_peer1 = tc::map_peer(smem_u32(&xs_full[1]), peer);
+    const uint8_t* xin = smem + OFF_XIN;
+    const uint8_t* pin = smem + OFF_PIN;
+    // The peer's buffers and barriers (messages are st.async stores that
+    // complete their bytes on the receiving CTA's barrier).
+    const uint32_t xin_peer = tc::map_peer(smem_u32(smem + OFF_XIN), peer);
+    const uint32_t pin_peer = tc::map_peer(smem_u32(smem + OFF_PIN), peer);
+    const uint32_t fin_peer = tc::map_peer(smem_u32(smem + OFF_FIN), peer);
+    const uint32_t xin_bar_peer0 = tc::map_peer(smem_u32(&xin_full[0]), peer);
+    const uint32_t pin_bar_peer0 = tc::map_peer(smem_u32(&pin_full[0]), peer);
+    const uint32_t fin_bar_peer = tc::map_peer(smem_u32(fin_full), peer);
     float m_used = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int n = 0; n < ntiles; ++n) {
-      const int bb = n & 1;             // exchange buffer
-      const uint32_t u = (n >> 1) & 1;  // its phase parity
-      if (!warp_wait(s_full, n & 1)) { ok = false; break; }
+
+    // Rescales this thread's O row (256 fp32 columns) by alpha once the
+    // previous P.V has completed; warp-uniform (lanes with alpha = 1 keep
+    // their values).
+    auto rescale_o = [&](int n, float alpha) -> bool {
+      if (!__any_sync(0xffffffffu, alpha != 1.f) || n == 0) return true;
+      if (!warp_wait(pv_done, (n - 1) & 1)) return false;
       tc::fence_after_sync();
-      uint32_t sr[64];
-      tc::ld_32x32b_x32(tmem + lane_base + S_COL,
-                        *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tc::ld_32x32b_x32(tmem + lane_base + S_COL + 32,
-                        *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tc::wait_ld();
-      tc::fence_before_sync();
-      mbar_arrive(s_free);
-      // partial S -> the peer's exchange buffer with st.async: each store
-      // completes its bytes on the peer's xs_full[bb]; one local thread
-      // announces the 128 x 64 x 4 bytes this CTA expects from the peer.
-      if (row_i == 0) mbar_arrive_expect_tx(&xs_full[bb], 128 * TBN * 4);
-      {
-        const uint32_t dst = xs_peer + bb * XS_BYTES;
-        const uint32_t pbar = bb ? xsbar_peer1 : xsbar_peer0;
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          tc::st_async_v4(dst + xs_off(row_i, j), __uint_as_float(sr[4 * j]),
-                          __uint_as_float(sr[4 * j + 1]), __uint_as_float(sr[4 * j + 2]),
-                          __uint_as_float(sr[4 * j + 3]), pbar);
-      }
-      const bool got = tc::mbar_wait_cluster(&xs_full[bb], u);
-      if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-      const uint8_t* xs = smem + OFF_XS + bb * XS_BYTES;
-      const int valid = min(TBN, end - (start + n * TBN));
-      float mt = -INFINITY;
-#pragma unroll
-      for (int j4 = 0; j4 < 16; ++j4) {
-        const float4 t = *reinterpret_cast<const float4*>(xs + xs_off(row_i, j4));
-        const float tv[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = 4 * j4 + e;
-          const float own = __uint_as_float(sr[j]);
-          // S = S_lo + S_hi on both CTAs (same operands, same bits)
-          const float s = rank == 0 ? own + tv[e] : tv[e] + own;
-          const float x = j < valid ? s * scale_log2 : -INFINITY;
-          sr[j] = __float_as_uint(x);
-          mt = fmaxf(mt, x);
-        }
-      }
-      const float m_new = fmaxf(m_used, mt);
-      const bool need = m_new > m_used + kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
-        const float alpha = ex2(m_used - m_new);
-        if (n > 0) {
-          if (!warp_wait(pv_done, (n - 1) & 1)) { ok = false; break; }
-          tc::fence_after_sync();
 #pragma unroll 1
-          for (int c = 0; c < 256; c += 32) {
-            uint32_t o[32];
-            tc::ld_32x32b_x32(tmem + lane_base + c, o);
-            tc::wait_ld();
+      for (int c = 0; c < 256; c += 32) {
+        uint32_t o[32];
+        tc::ld_32x32b_x32(tmem + lane_base + c, o);
+        tc::wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tc::st_32x32b_x32(tmem + lane_base + c, o);
-          }
-          tc::wait_st();
-        }
-        l_run *= alpha;
-        m_used = m_new;
+        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+        tc::st_32x32b_x32(tmem + lane_base + c, o);
       }
-      uint32_t pk[32];
-      float psum = 0.f;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float a0 = ex2(__uint_as_float(sr[2 * j]) - m_used);
-        const float a1 = ex2(__uint_as_float(sr[2 * j + 1]) - m_used);
-        psum += a0 + a1;
-        pk[j] = pack_bf16x2(a0, a1);
-      }
-      l_run += psum;
-      // P's TMEM columns are free once the previous P.V has completed
-      if (n >= 1 && !warp_wait(pv_done, (n - 1) & 1)) { ok = false; break; }
+      tc::wait_st();
+      return true;
+    };
+    // Stores P into TMEM once the previous P.V has released the columns.
+    auto store_p = [&](int n, const uint32_t (&pk)[32]) -> bool {
+      if (n >= 1 && !warp_wait(pv_done, (n - 1) & 1)) return false;
       tc::fence_after_sync();
       tc::st_32x32b_x32(tmem + lane_base + P_COL, pk);
       tc::wait_st();
       tc::fence_before_sync();
       mbar_arrive(p_full);
+      return true;
+    };
+    // Loads S_n into sr once the MMA has produced it and frees its columns.
+    auto load_s = [&](int n, uint32_t (&sr)[64]) -> bool {
+      if (!warp_wait(s_full, n & 1)) return false;
+      tc::fence_after_sync();
+      tc::ld_32x32b_x32(tmem + lane_base + S_COL, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tc::ld_32x32b_x32(tmem + lane_base + S_COL + 32,
+                        *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tc::wait_ld();
+      tc::fence_before_sync();
+      mbar_arrive(s_free);
+      return true;
+    };
+
+    if (!own) {
+      // Forwarding rows.  Each warp stores the P of tile np as soon as it
+      // has come back (first: it gates the P.V that frees a KV stage) and
+      // sends its rows' partial scores of tile ns as soon as S is there.
+      // Partial ns goes into the peer's buffer ns & 1, which the peer has
+      // read once it returned the P of tile ns - 2: hence ns <= np + 1.
+      int ns = 0, np = 0;
+      uint64_t t_idle = 0;
+      uint32_t spins = 0;
+      while (np < ntiles) {
+        bool did = false;
+        if (np < ns &&
+            __shfl_sync(0xffffffffu, tc::mbar_test_cluster(&pin_full[np & 1], (np >> 1) & 1),
+                        0)) {
+          const uint8_t* src = pin + (np & 1) * XP_BYTES;
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 x = *reinterpret_cast<const uint4*>(src + xoff(xi, j, XP_ROW));
+            pk[4 * j] = x.x;
+            pk[4 * j + 1] = x.y;
+            pk[4 * j + 2] = x.z;
+            pk[4 * j + 3] = x.w;
+          }
+          const float alpha = reinterpret_cast<const float*>(src + XP_ALPHA)[xi];
+          if (!rescale_o(np, alpha)) { ok = false; break; }
+          if (!store_p(np, pk)) { ok = false; break; }
+          ++np;
+          did = true;
+        }
+        if (ns < ntiles && ns <= np + 1 &&
+            __shfl_sync(0xffffffffu, mbar_test(s_full, ns & 1), 0)) {
+          uint32_t sr[64];
+          if (!load_s(ns, sr)) { ok = false; break; }
+          const int bb = ns & 1;
+          if (lead) mbar_arrive_expect_tx(&pin_full[bb], XP_BYTES);  // P of tile ns
+          const uint32_t dst = xin_peer + bb * XS_BYTES;
+          const uint32_t bar = xin_bar_peer0 + bb * 8;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            tc::st_async_v4u(dst + xoff(xi, j, XS_ROW), sr[4 * j], sr[4 * j + 1], sr[4 * j + 2],
+                             sr[4 * j + 3], bar);
+          ++ns;
+          did = true;
+        }
+        if (did) {
+          t_idle = 0;
+          spins = 0;
+        } else if ((++spins & 1023u) == 0) {
+          const uint64_t now = globaltimer();
+          if (t_idle == 0) {
+            t_idle = now;
+          } else if (now - t_idle > kWaitTimeoutNs) {
+            ok = false;
+            break;
+          }
+        }
+      }
+    } else {
+      for (int n = 0; n < ntiles && ok; ++n) {
+        const int bb = n & 1;              // exchange buffer
+        const uint32_t u = (n >> 1) & 1;   // its phase parity
+        uint32_t sr[64];
+        if (!load_s(n, sr)) { ok = false; break; }
+        // ---- add the peer's partial scores for this row (xin[bb] is not
+        // rewritten before the peer has received this tile's P)
+        if (lead) mbar_arrive_expect_tx(&xin_full[bb], XS_BYTES);
+        if (!warp_wait_cluster(&xin_full[bb], u)) { ok = false; break; }
+        const uint8_t* src = xin + bb * XS_BYTES;
+        const int valid = min(TBN, end - (start + n * TBN));
+        float mt = -INFINITY;
+#pragma unroll
+        for (int j4 = 0; j4 < 16; ++j4) {
+          const float4 t = *reinterpret_cast<const float4*>(src + xoff(xi, j4, XS_ROW));
+          const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * j4 + e;
+            const float s = __uint_as_float(sr[j]) + tv[e];
+            const float x = j < valid ? s * scale_log2 : -INFINITY;
+            sr[j] = __float_as_uint(x);
+            mt = fmaxf(mt, x);
+          }
+        }
+        // ---- online softmax with lazy rescaling
+        const float m_new = fmaxf(m_used, mt);
+        float alpha = 1.f;
+        if (m_new > m_used + kRescaleThreshold) {
+          alpha = n > 0 ? ex2(m_used - m_new) : 1.f;
+          l_run *= alpha;
+          m_used = m_new;
+        }
+        uint32_t pk[32];
+        float psum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float a0 = ex2(__uint_as_float(sr[2 * j]) - m_used);
+          const float a1 = ex2(__uint_as_float(sr[2 * j + 1]) - m_used);
+          psum[j & 3] += a0 + a1;
+          pk[j] = pack_bf16x2(a0, a1);
+        }
+        l_run += (psum[0] + psum[1]) + (psum[2] + psum[3]);
+        // ---- P and alpha to the peer, for its half of O (its buffer bb
+        // held the P of tile n - 2, which it has stored: it sent this
+        // tile's partial scores only afterwards)
+        {
+          const uint32_t dst = pin_peer + bb * XP_BYTES;
+          const uint32_t bar = pin_bar_peer0 + bb * 8;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            tc::st_async_v4u(dst + xoff(xi, j, XP_ROW), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                             pk[4 * j + 3], bar);
+          tc::st_async_b32(dst + XP_ALPHA + 4 * xi, __float_as_uint(alpha), bar);
+        }
+        if (!rescale_o(n, alpha)) { ok = false; break; }
+        if (!store_p(n, pk)) { ok = false; break; }
+      }
+    }
+
+    // ---- the owner's 1 / l reaches the other CTA as a last message
+    float inv = 0.f;
+    if (ok) {
+      if (own) {
+        inv = 1.f / l_run;
+        tc::st_async_b32(fin_peer + 4 * xi, __float_as_uint(inv), fin_bar_peer);
+      } else {
+        if (lead) mbar_arrive_expect_tx(fin_full, 64 * 4);
+        if (warp_wait_cluster(fin_full, 0))
+          inv = reinterpret_cast<const float*>(smem + OFF_FIN)[xi];
+        else
+          ok = false;
+      }
     }
     if (!ok) {
       if (lane == 0 && p.err_count) atomicAdd(p.err_count, kTimeoutErr);
@@ -418,10 +617,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       const bool valid_v = v < nvec;
       const int row = valid_v ? b * p.rows_per_seq + v / H : 0;
       const int h = valid_v ? v % H : 0;
-      const float inv = 1.f / l_run;
-      float lg;
-      asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(l_run));
-      const float lse = (m_used + lg) * kLn2;
       const int64_t rec = (static_cast<int64_t>(row) * S + s0) * H + h;
 #pragma unroll 1
       for (int c = 0; c < 256; c += 32) {
@@ -448,7 +643,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
                             __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
         }
       }
-      if (valid_v && rank == 0) {
+      if (valid_v && own) {
+        float lg;
+        asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(l_run));
+        const float lse = (m_used + lg) * kLn2;
         if (S == 1) {
           p.lse[static_cast<int64_t>(row) * H + h] = lse;
         } else {
@@ -467,7 +665,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::cluster_sync();  // no CTA leaves while its peer may still write to it
-  if (warp == 5) {
+  if (warp == mma_warp) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, TMEM_COLS);
   }

@@ -194,12 +194,54 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, floa
       "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
       : "memory");
 }
+__device__ __forceinline__ void st_async_v4u(uint32_t cluster_addr, uint32_t a, uint32_t b,
+                                             uint32_t c, uint32_t d, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], "
+      "{%1, %2, %3, %4}, [%5];" ::"r"(cluster_addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t a,
+                                             uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+          cluster_addr),
+      "r"(a), "r"(cluster_bar)
+      : "memory");
+}
+// Non-blocking test (acquire at cluster scope) of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 
 }  // namespace tc
 }  // namespace mla
 
 namespace mla {
 namespace tc {
+
+// Copies `bytes` (a multiple of 16) from this CTA's shared memory to the
+// shared memory of another CTA of the cluster (`dst` and `bar` are cluster
+// addresses there); the copy completes `bytes` of the transaction count of
+// that CTA's mbarrier `bar`.  The source must be made visible to the async
+// proxy (fence_proxy_async_smem) by the threads that wrote it.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 
 // D[tmem] (+)= A[tmem] * B[smem]: A is M lanes x K columns of packed 16-bit
 // pairs (lane m, column k/2, low half = even k); issued by one thread.
