@@ -26,21 +26,28 @@
 // TMEM (512 columns): O [0, 256), S [256, 320), P [320, 352) as packed
 // bf16, Q [352, 512) as packed bf16 (rank 1 needs 160 columns for its 320
 // dims).  Q and P are A operands read straight from TMEM by the MMAs; only K
-// and V tiles and the exchange buffers live in shared memory.  The ring is
-// short (4 stages of 64 tokens), so the producer also prefetches the tiles
-// a few steps ahead into L2.
+// and V tiles (a 4-stage ring of 64 tokens) and the exchange buffers live in
+// shared memory.
 //
 // Roles per CTA (256 threads):
-//   warps 0-3  softmax: thread i owns TMEM lane i = query vector i.  The two
-//              warps of the vectors this CTA owns run the softmax (row max
-//              and sum thread-local, lazy rescaling of O only when the
-//              running max grows by more than 2^8); the other two forward
-//              their rows' partial scores and store the P they get back;
+//   softmax: thread = TMEM lane = query vector.  The 64 vectors the peer
+//              owns are forwarded by the two warps of their lane quarters
+//              (partial scores out, P and the rescale factor in, whichever
+//              is ready); the 64 this CTA owns get four warps, two per lane
+//              quarter, each taking one half of the 64 tokens, which share
+//              the row maximum and sum through shared memory (lazy
+//              rescaling of O only when the running max grows by more than
+//              2^8);
 //   one warp   MMA issuer (one thread) and TMEM owner;
 //   one warp   TMA producer: 64-token tiles of the paged cache into a
-//              4-stage mbarrier ring (128-byte swizzled boxes);
-//   the MMA and producer warps sit on the sub-partitions of the forwarding
-//   warps (the two remaining warps only join the final barrier).
+//              4-stage mbarrier ring (128-byte swizzled boxes).
+//   The MMA and producer warps sit on the lane quarters (sub-partitions) of
+//   the forwarding warps, the lighter softmax work.
+//
+// With several splits the kernel is persistent: one CTA pair per two SMs
+// takes an equal share of all tiles of all (sequence, 128-vector block)
+// units, cut into segments at unit boundaries, each segment yielding one
+// partial (o, lse) in the unit's next split slot.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -54,7 +61,6 @@ namespace {
 
 constexpr int TBN = 64;                   // tokens per tile
 constexpr int TSTAGES = 4;                // KV ring depth
-constexpr int TPREFETCH = 4;              // tiles fetched into L2 ahead of the ring
 constexpr int TMAXCH = 5;                 // max 64-dim chunks per CTA
 constexpr int CHUNK_BYTES = TBN * 128;    // one 64-dim box of a tile (8 KiB)
 constexpr int STAGE_BYTES = TMAXCH * CHUNK_BYTES;
@@ -67,8 +73,11 @@ constexpr int OFF_STAGE = 0;
 constexpr int OFF_XIN = OFF_STAGE + TSTAGES * STAGE_BYTES;  // peer partials, x2
 constexpr int OFF_PIN = OFF_XIN + 2 * XS_BYTES;             // P from the peer, x2
 constexpr int OFF_FIN = OFF_PIN + 2 * XP_BYTES;             // 1 / l from the peer
-constexpr int OFF_BAR = OFF_FIN + 256;
-constexpr int NBARS = 2 * TSTAGES + 5 + 5;
+constexpr int OFF_RED = OFF_FIN + 256;                      // own rows: max / sum exchange
+constexpr int OFF_PRE = OFF_RED + 6 * 64 * 4;               // schedule: unit tile prefix
+constexpr int OFF_LEN = OFF_PRE + (kMaxPersistUnits + 1) * 4;  // schedule: sequence lengths
+constexpr int OFF_BAR = (OFF_LEN + kMaxPersistUnits * 4 + 7) & ~7;
+constexpr int NBARS = 2 * TSTAGES + 5 + 8;
 constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
 constexpr int TC_SMEM = OFF_TMEMSLOT + 16 + 1024;  // + alignment slack
 constexpr int TC_THREADS = 256;
@@ -103,9 +112,21 @@ __device__ __forceinline__ uint32_t xoff(uint32_t r, uint32_t c, uint32_t row_by
   return r * row_bytes + ((c ^ (r & 7u)) << 4);
 }
 
+// One unit of work of a CTA pair: tokens [start, end) of sequence b for the
+// 128-vector block g, whose result goes to split slot `slot` (or straight to
+// o / lse when `direct`).  `mark_lo..mark_hi` are slots this segment marks
+// unused (lse = -inf): fused splits in grid mode, or the slots a unit's
+// partition leaves free (written by its first segment) in persistent mode.
+struct TcSeg {
+  int b, g, start, end, slot, mark_lo, mark_hi;
+  bool direct;
+};
+
+constexpr int kClampedBit = 1 << 30;
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap,
-                     const int split_group) {
+                     const int split_group, const int persistent) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -119,8 +140,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   uint64_t* mma_done = s_full + 4;
   uint64_t* xin_full = s_full + 5;   // [2] peer partial scores landed
   uint64_t* pin_full = s_full + 7;   // [2] peer P landed
-  uint64_t* fin_full = s_full + 9;   // peer's 1 / l landed
+  uint64_t* fin_full = s_full + 9;   // peer's 1 / l landed (one per segment)
+  uint64_t* q_ready = s_full + 10;   // Q of the segment is in TMEM
+  uint64_t* o_free = s_full + 11;    // the segment's O has been read out
+  uint64_t* own_bar = s_full + 12;   // the four warps of this CTA's own rows
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEMSLOT);
+  int* pre = reinterpret_cast<int*>(smem + OFF_PRE);
+  int* lens = reinterpret_cast<int*>(smem + OFF_LEN);
 
   const uint32_t rank = tc::cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
@@ -132,53 +158,139 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   // the softmax: warps 2, 3 forward on rank 0, warps 0, 1 on rank 1.
   const int mma_warp = rank == 0 ? 6 : 4;
   const int prod_warp = mma_warp + 1;
-  const int g_blk = blockIdx.x >> 1, ysplit = blockIdx.y, b = blockIdx.z;
   const int H = p.num_heads;
   const int nvec = p.rows_per_seq * H;
-  const int v0 = g_blk * 128;
+  const int qblocks = cdiv(nvec, 128);
   const int S = p.num_splits;
+  const int Lmax = p.max_blocks * p.block_size;
   if (threadIdx.x == 128) tma_prefetch_desc(&tmap);
   // Launched overlapped with the previous kernel of the stream: nothing in
   // global memory is read before it has completed.
   griddep_wait();
   griddep_launch_dependents();
 
-  int L = __ldg(p.seq_lens + b);
-  const int Lmax = p.max_blocks * p.block_size;
-  if (L < 0) L = 0;
-  if (L > Lmax) {
-    if (threadIdx.x == 0 && rank == 0 && ysplit == 0 && g_blk == 0 && p.err_count)
-      atomicAdd(p.err_count, 1);
-    L = Lmax;
-  }
-  const int per = L > 0 ? cdiv(cdiv(L, S), 64) * 64 : 64;
-  const int s0 = ysplit * split_group;
-  const int s1 = min(S, s0 + split_group);
-  const int start = s0 * per;
-  const int end = min(L, s1 * per);
-  const int ntiles = start < end ? cdiv(end - start, TBN) : 0;
-
-  if (ntiles == 0) {
-    // Both CTAs of the pair take this branch together.
-    if (threadIdx.x < 128) {
-      const int v = v0 + threadIdx.x;
-      if (v < nvec) {
-        const int row = b * p.rows_per_seq + v / H, h = v % H;
-        if (S == 1) {
-          // Empty sequence in single-pass mode: o = 0, lse = -inf.
-          uint16_t* orow = p.o + (static_cast<int64_t>(row) * H + h) * 512 + rank * 256;
-          for (int c = 0; c < 256; c += 8)
-            *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-          if (rank == 0) p.lse[static_cast<int64_t>(row) * H + h] = -INFINITY;
-        } else if (L > 0 && rank == 0) {
-          // Splits past the end of a non-empty sequence: no partial.
-          for (int s = s0; s < s1; ++s)
-            p.ws_lse[(static_cast<int64_t>(row) * S + s) * H + h] = -INFINITY;
+  // ---------------------------------------------------------- schedule
+  // Persistent: the tiles of all units (sequence, 128-vector block) form one
+  // list; pair c takes tiles [c * C, (c + 1) * C), cut into segments at unit
+  // boundaries (the same walk as the warp-MMA kernel's).  Grid: one segment
+  // per pair, split_group consecutive splits of one unit.
+  int units = 0, C = 1, lo = 0, hi = 0, cidx = 0;
+  TcSeg gseg{};
+  int nseg = 0;
+  if (persistent) {
+    cidx = blockIdx.x >> 1;
+    units = p.num_seqs * qblocks;
+    for (int u = threadIdx.x; u < units; u += blockDim.x) {
+      const int b = u / qblocks;
+      const int raw = __ldg(p.seq_lens + b);
+      const int L = raw < 0 ? 0 : (raw > Lmax ? Lmax : raw);
+      pre[u + 1] = cdiv(L, TBN);
+      if (u == b * qblocks) lens[b] = L | (raw > Lmax ? kClampedBit : 0);
+    }
+    if (threadIdx.x == 0) pre[0] = 0;
+    __syncthreads();
+    __shared__ int s_max;
+    if (warp == 0) {
+      int carry = 0, mx = 0;
+      for (int base = 1; base <= units; base += 32) {
+        const int i = base + lane;
+        int v = i <= units ? pre[i] : 0;
+        mx = max(mx, v);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += t;
+        }
+        if (i <= units) pre[i] = v + carry;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0) s_max = mx;
+    }
+    __syncthreads();
+    const int total = pre[units];
+    const int npairs = gridDim.x >> 1;
+    C = max(max(cdiv(total, npairs), cdiv(s_max, max(S - 1, 1))), 1);
+    lo = cidx * C;
+    hi = min(total, lo + C);
+    if (lo >= hi) return;  // both CTAs of the pair leave together
+  } else {
+    const int b = blockIdx.z, ysplit = blockIdx.y;
+    int L = __ldg(p.seq_lens + b);
+    if (L < 0) L = 0;
+    if (L > Lmax) {
+      if (threadIdx.x == 0 && rank == 0 && ysplit == 0 && (blockIdx.x >> 1) == 0 && p.err_count)
+        atomicAdd(p.err_count, 1);
+      L = Lmax;
+    }
+    const int per = L > 0 ? cdiv(cdiv(L, S), 64) * 64 : 64;
+    const int s0 = ysplit * split_group;
+    const int s1 = min(S, s0 + split_group);
+    gseg.b = b;
+    gseg.g = blockIdx.x >> 1;
+    gseg.start = s0 * per;
+    gseg.end = min(L, s1 * per);
+    gseg.slot = s0;
+    gseg.mark_lo = s0 + 1;
+    gseg.mark_hi = s1;
+    gseg.direct = S == 1;
+    if (gseg.start >= gseg.end) {
+      // Both CTAs of the pair take this branch together.
+      if (threadIdx.x < 128) {
+        const int v = gseg.g * 128 + threadIdx.x;
+        if (v < nvec) {
+          const int row = b * p.rows_per_seq + v / H, h = v % H;
+          if (S == 1) {
+            // Empty sequence in single-pass mode: o = 0, lse = -inf.
+            uint16_t* orow = p.o + (static_cast<int64_t>(row) * H + h) * 512 + rank * 256;
+            for (int c = 0; c < 256; c += 8)
+              *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+            if (rank == 0) p.lse[static_cast<int64_t>(row) * H + h] = -INFINITY;
+          } else if (L > 0 && rank == 0) {
+            // Splits past the end of a non-empty sequence: no partial.
+            for (int s = s0; s < s1; ++s)
+              p.ws_lse[(static_cast<int64_t>(row) * S + s) * H + h] = -INFINITY;
+          }
         }
       }
+      return;
     }
-    return;
+    nseg = 1;
   }
+  // Walks this pair's segments in order, calling f(seg, index, first tile).
+  auto for_each_seg = [&](auto&& f) {
+    if (!persistent) {
+      if (nseg) f(gseg, 0, 0);
+      return;
+    }
+    int a = 0, z = units;  // first unit with pre[u + 1] > lo
+    while (a < z) {
+      const int m = (a + z) >> 1;
+      if (pre[m + 1] > lo) z = m; else a = m + 1;
+    }
+    int k = 0, n0 = 0;
+    for (int u = a; u < units && pre[u] < hi; ++u) {
+      const int t_lo = max(lo, pre[u]) - pre[u], t_hi = min(hi, pre[u + 1]) - pre[u];
+      if (t_hi <= t_lo) continue;
+      TcSeg s;
+      s.b = u / qblocks;
+      s.g = u - s.b * qblocks;
+      const int L = lens[s.b] & ~kClampedBit;
+      s.start = t_lo * TBN;
+      s.end = min(L, t_hi * TBN);
+      const int cf = pre[u] / C;
+      s.slot = cidx - cf;
+      s.mark_lo = s.slot == 0 ? (pre[u + 1] - 1) / C - cf + 1 : S;
+      s.mark_hi = S;
+      s.direct = false;
+      if (s.slot == 0 && s.g == 0 && (lens[s.b] & kClampedBit) && threadIdx.x == 0 &&
+          rank == 0 && p.err_count)
+        atomicAdd(p.err_count, 1);  // seq_len beyond the block table, once per sequence
+      if (!f(s, k++, n0)) return;
+      n0 += t_hi - t_lo;
+    }
+  };
 
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
@@ -187,8 +299,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       mbar_init(&kv_empty[i], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 128);
-    mbar_init(p_full, 128);
+    // S / P / Q / O hand-offs: 64 forwarding + 128 own-row threads
+    mbar_init(s_free, 192);
+    mbar_init(p_full, 192);
     mbar_init(pv_done, 1);
     mbar_init(mma_done, 1);
     for (int i = 0; i < 2; ++i) {
@@ -196,6 +309,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       mbar_init(&pin_full[i], 1);
     }
     mbar_init(fin_full, 1);
+    mbar_init(q_ready, 192);
+    mbar_init(o_free, 192);
+    mbar_init(own_bar, 128);
     fence_mbar_init();
   }
   if (warp == mma_warp) {
@@ -207,34 +323,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   tc::cluster_sync();  // the peer's barriers exist before any remote traffic
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  if (warp < 4) {
-    // Q: thread i puts its vector's dims [64*c0, 64*(c0+nch)) into TMEM lane
-    // i as packed bf16 pairs (padding vectors are zeros).
-    const int v = v0 + threadIdx.x;
-    const uint16_t* src = nullptr;
-    if (v < nvec) {
-      const int row = b * p.rows_per_seq + v / H, h = v % H;
-      src = p.q + row * p.q_row_stride + h * p.q_head_stride + c0 * 64;
-    }
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    for (int c = 0; c < nch; ++c) {
-      uint32_t r[32];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint4 x = src ? __ldg(reinterpret_cast<const uint4*>(src + c * 64) + j)
-                            : make_uint4(0, 0, 0, 0);
-        r[4 * j] = x.x;
-        r[4 * j + 1] = x.y;
-        r[4 * j + 2] = x.z;
-        r[4 * j + 3] = x.w;
-      }
-      tc::st_32x32b_x32(tmem + lane_base + Q_COL + c * 32, r);
-    }
-    tc::wait_st();
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
   const uint32_t stage_base = smem_u32(smem + OFF_STAGE);
 
   if (warp == prod_warp) {
@@ -243,186 +331,188 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       const int bs = p.block_size;
       const int rows_box = bs < TBN ? bs : TBN;
       const int npg = TBN / rows_box;
-      const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-      // Block ids of tile t (pages past the split end read as 0; they are
-      // neither loaded nor prefetched).
-      auto ids_of = [&](int t, int (&ids)[4]) {
+      int n = 0;  // tiles issued (ring position)
+      for_each_seg([&](const TcSeg& sg, int, int) -> bool {
+        const int32_t* bt = p.block_table + static_cast<int64_t>(sg.b) * p.bt_stride;
+        const int ntiles = cdiv(sg.end - sg.start, TBN);
+        // Block ids of tile t of the segment (pages past its end read as 0
+        // and are not loaded).
+        auto ids_of = [&](int t, int (&ids)[4]) {
 #pragma unroll
-        for (int pg = 0; pg < 4; ++pg) {
-          const int tk = start + t * TBN + pg * rows_box;
-          ids[pg] = (pg < npg && t < ntiles && tk < end) ? __ldg(bt + tk / bs) : 0;
+          for (int pg = 0; pg < 4; ++pg) {
+            const int tk = sg.start + t * TBN + pg * rows_box;
+            ids[pg] = (pg < npg && t < ntiles && tk < sg.end) ? __ldg(bt + tk / bs) : 0;
+          }
+        };
+        auto pages_of = [&](int t) {
+          int np = 0;
+          for (int pg = 0; pg < npg; ++pg)
+            if (sg.start + t * TBN + pg * rows_box < sg.end) ++np;
+          return t < ntiles ? np : 0;
+        };
+        // Ids are read one tile before they are used, so the block-table
+        // latency hides behind a tile's worth of waiting.
+        int cur[4], nxt[4];
+        ids_of(0, cur);
+        for (int t = 0; t < ntiles; ++t, ++n) {
+          ids_of(t + 1, nxt);
+          const int st = n % TSTAGES;
+          const uint32_t ph = (n / TSTAGES) & 1;
+          if (!mbar_wait(&kv_empty[st], ph ^ 1)) {
+            if (p.err_count) atomicAdd(p.err_count, kTimeoutErr);
+            return false;
+          }
+          const int npages = pages_of(t);
+          mbar_arrive_expect_tx(&kv_full[st],
+                                static_cast<uint32_t>(npages * nch * rows_box * 128));
+          uint8_t* dst = smem + OFF_STAGE + st * STAGE_BYTES;
+#pragma unroll
+          for (int pg = 0; pg < 4; ++pg) {
+            if (pg >= npages) break;
+            const int tk = sg.start + t * TBN + pg * rows_box;
+            const int blk = cur[pg];
+            const int row0 = tk % bs;
+            if ((blk < 0 || blk >= p.num_blocks) && p.err_count && rank == 0)
+              atomicAdd(p.err_count, 1);
+            for (int cl = 0; cl < nch; ++cl)
+              tma_load_3d(dst + cl * CHUNK_BYTES + pg * rows_box * 128, &tmap,
+                          &kv_full[st], (c0 + cl) * 64, row0, blk);
+          }
+#pragma unroll
+          for (int pg = 0; pg < 4; ++pg) cur[pg] = nxt[pg];
         }
-      };
-      auto pages_of = [&](int t) {
-        int n = 0;
-        for (int pg = 0; pg < npg; ++pg)
-          if (start + t * TBN + pg * rows_box < end) ++n;
-        return t < ntiles ? n : 0;
-      };
-      auto prefetch = [&](const int (&ids)[4], int t) {
-        const int np = pages_of(t);
-#pragma unroll
-        for (int pg = 0; pg < 4; ++pg) {
-          if (pg >= np) break;
-          if (ids[pg] < 0 || ids[pg] >= p.num_blocks) continue;
-          const int row0 = (start + t * TBN + pg * rows_box) % bs;
-          for (int cl = 0; cl < nch; ++cl)
-            tma_prefetch_l2_3d(&tmap, (c0 + cl) * 64, row0, ids[pg]);
-        }
-      };
-      // Ids are read one tile before they are used, so the block-table
-      // latency hides behind a tile's worth of waiting.
-      int cur[4], nxt[4], pf[4], first[TPREFETCH][4];
-      ids_of(0, cur);
-#pragma unroll
-      for (int t = 0; t < TPREFETCH; ++t) ids_of(t + 1, first[t]);
-      ids_of(TPREFETCH + 1, pf);
-      for (int n = 0; n < ntiles; ++n) {
-        ids_of(n + 1, nxt);
-        const int st = n % TSTAGES;
-        const uint32_t ph = (n / TSTAGES) & 1;
-        if (!mbar_wait(&kv_empty[st], ph ^ 1)) {
-          if (p.err_count) atomicAdd(p.err_count, kTimeoutErr);
-          break;
-        }
-        const int npages = pages_of(n);
-        mbar_arrive_expect_tx(&kv_full[st],
-                              static_cast<uint32_t>(npages * nch * rows_box * 128));
-        uint8_t* dst = smem + OFF_STAGE + st * STAGE_BYTES;
-#pragma unroll
-        for (int pg = 0; pg < 4; ++pg) {
-          if (pg >= npages) break;
-          const int t = start + n * TBN + pg * rows_box;
-          const int blk = cur[pg];
-          const int row0 = t % bs;
-          if ((blk < 0 || blk >= p.num_blocks) && p.err_count && rank == 0)
-            atomicAdd(p.err_count, 1);
-          for (int cl = 0; cl < nch; ++cl)
-            tma_load_3d(dst + cl * CHUNK_BYTES + pg * rows_box * 128, &tmap,
-                        &kv_full[st], (c0 + cl) * 64, row0, blk);
-        }
-        if (n == 0) {
-          // tiles 1 .. TPREFETCH, once the first tile's loads are on their way
-#pragma unroll
-          for (int t = 0; t < TPREFETCH; ++t) prefetch(first[t], t + 1);
-        }
-        // L2 prefetch of tile n + 1 + TPREFETCH (ids read one tile ago)
-        prefetch(pf, n + 1 + TPREFETCH);
-        ids_of(n + 2 + TPREFETCH, pf);
-#pragma unroll
-        for (int pg = 0; pg < 4; ++pg) cur[pg] = nxt[pg];
-      }
+        return true;
+      });
     }
   } else if (warp == mma_warp) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idS = tc::idesc_bf16(128, TBN, 0, 0);
     constexpr uint32_t idPV = tc::idesc_bf16(128, 256, 0, 1);
-    // S of tile n needs its KV stage and the S columns (every softmax thread
-    // has read S of tile n - 1); P.V of tile k needs P of tile k.  The two
-    // streams are issued as soon as each is ready, so S runs ahead of the
-    // P round trip between the CTAs.
-    int ns = 0, npv = 0;
+    // S of tile n needs its KV stage, the S columns (every softmax thread
+    // has read S of tile n - 1) and, first in a segment, the segment's Q;
+    // P.V of tile n needs P of tile n and, first in a segment, the previous
+    // segment's O read out.  Within a segment the two streams are issued as
+    // soon as each is ready (P.V first), so S runs ahead of the P round trip
+    // between the CTAs.
     bool ok = true;
-    uint64_t t_idle = 0;
-    uint32_t spins = 0;
-    while (npv < ntiles) {
-      bool progress = false;
-      // P.V first: it releases a KV stage and the P columns.  (Lane 0
-      // decides, so the warp stays converged.)
-      const bool pv_ready = __shfl_sync(0xffffffffu, npv < ns && mbar_test(p_full, npv & 1), 0);
-      if (pv_ready) {
-        tc::fence_after_sync();
-        if (lane == 0) {
-          // A = P (TMEM, 16 tokens = 8 packed columns per step); B = V:
-          // MN-major, 128-byte swizzle (N step = next 64-dim box, K step = 8
-          // tokens = 1024 B; 16 tokens per MMA = 2048 B = 128 in the field).
-          const uint64_t d0 = tc::smem_desc(stage_base + (npv % TSTAGES) * STAGE_BYTES,
-                                            CHUNK_BYTES, 1024, tc::kLayoutSw128);
+    int ns = 0, npv = 0;  // global tile counters
+    for_each_seg([&](const TcSeg& sg, int k, int n0) -> bool {
+      const int n1 = n0 + cdiv(sg.end - sg.start, TBN);
+      uint64_t t_idle = 0;
+      uint32_t spins = 0;
+      bool have_q = false, have_o = k == 0;
+      while (npv < n1) {
+        bool progress = false;
+        // (lane 0 decides, so the warp stays converged)
+        if (!have_o) have_o = __shfl_sync(0xffffffffu, mbar_test(o_free, (k - 1) & 1), 0);
+        const bool pv_ready =
+            have_o && __shfl_sync(0xffffffffu, npv < ns && mbar_test(p_full, npv & 1), 0);
+        if (pv_ready) {
+          tc::fence_after_sync();
+          if (lane == 0) {
+            // A = P (TMEM, 16 tokens = 8 packed columns per step); B = V:
+            // MN-major, 128-byte swizzle (N step = next 64-dim box, K step =
+            // 8 tokens = 1024 B; 16 tokens per MMA = 2048 B = 128 in the
+            // descriptor's address field).
+            const uint64_t d0 = tc::smem_desc(stage_base + (npv % TSTAGES) * STAGE_BYTES,
+                                              CHUNK_BYTES, 1024, tc::kLayoutSw128);
 #pragma unroll
-          for (int kk = 0; kk < TBN / 16; ++kk)
-            tc::mma_ts(tmem, tmem + P_COL + kk * 8, d0 + static_cast<uint64_t>(kk * 128), idPV,
-                       (npv > 0 || kk > 0) ? 1u : 0u);
-          tc::commit(pv_done);
-          tc::commit(&kv_empty[npv % TSTAGES]);
-        }
-        __syncwarp();
-        ++npv;
-        progress = true;
-      }
-      const bool s_ready = __shfl_sync(
-          0xffffffffu,
-          ns < ntiles && mbar_test(&kv_full[ns % TSTAGES], (ns / TSTAGES) & 1) &&
-              (ns == 0 || mbar_test(s_free, (ns - 1) & 1)),
-          0);
-      if (s_ready) {
-        const int st = ns % TSTAGES;
-        const int valid = min(TBN, end - (start + ns * TBN));
-        if (valid < TBN) {
-          // Rows past the split end hold other tokens or NaN: zero them so
-          // the P.V product sees 0 * 0 there (their scores are masked).
-          uint8_t* stp = smem + OFF_STAGE + st * STAGE_BYTES;
-          const int nz = (TBN - valid) * nch * 8;
-          for (int i = lane; i < nz; i += 32) {
-            const int r = valid + i / (nch * 8), rem = i % (nch * 8);
-            *reinterpret_cast<uint4*>(stp + (rem >> 3) * CHUNK_BYTES + r * 128 +
-                                      (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+            for (int kk = 0; kk < TBN / 16; ++kk)
+              tc::mma_ts(tmem, tmem + P_COL + kk * 8, d0 + static_cast<uint64_t>(kk * 128),
+                         idPV, (npv > n0 || kk > 0) ? 1u : 0u);
+            tc::commit(pv_done);
+            tc::commit(&kv_empty[npv % TSTAGES]);
           }
-          fence_proxy_async_smem();
           __syncwarp();
+          ++npv;
+          progress = true;
         }
-        tc::fence_after_sync();
-        if (lane == 0) {
-          // S = Q K^T: A = Q from TMEM (16 dims = 8 packed columns per
-          // step), B = K tile, K-major with 128-byte swizzle.  The
-          // descriptor's start-address field (bytes / 16) is advanced by
-          // addition: one 64-dim box is CHUNK_BYTES / 16, one 16-dim step 2.
-          const uint64_t d0 =
-              tc::smem_desc(stage_base + st * STAGE_BYTES, 16, 1024, tc::kLayoutSw128);
-#pragma unroll 1
-          for (int c = 0; c < nch; ++c) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const int ks = c * 4 + kk;
-              tc::mma_ts(tmem + S_COL, tmem + Q_COL + ks * 8,
-                         d0 + static_cast<uint64_t>(c * (CHUNK_BYTES >> 4) + kk * 2), idS,
-                         ks > 0 ? 1u : 0u);
+        if (!have_q) have_q = __shfl_sync(0xffffffffu, mbar_test(q_ready, k & 1), 0);
+        const bool s_ready =
+            have_q && __shfl_sync(0xffffffffu,
+                                  ns < n1 &&
+                                      mbar_test(&kv_full[ns % TSTAGES], (ns / TSTAGES) & 1) &&
+                                      (ns == 0 || mbar_test(s_free, (ns - 1) & 1)),
+                                  0);
+        if (s_ready) {
+          const int st = ns % TSTAGES;
+          const int valid = min(TBN, sg.end - (sg.start + (ns - n0) * TBN));
+          if (valid < TBN) {
+            // Rows past the segment end hold other tokens or NaN: zero them
+            // so the P.V product sees 0 * 0 there (their scores are masked).
+            uint8_t* stp = smem + OFF_STAGE + st * STAGE_BYTES;
+            const int nz = (TBN - valid) * nch * 8;
+            for (int i = lane; i < nz; i += 32) {
+              const int r = valid + i / (nch * 8), rem = i % (nch * 8);
+              *reinterpret_cast<uint4*>(stp + (rem >> 3) * CHUNK_BYTES + r * 128 +
+                                        (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
             }
+            fence_proxy_async_smem();
+            __syncwarp();
           }
-          tc::commit(s_full);
+          tc::fence_after_sync();
+          if (lane == 0) {
+            // S = Q K^T: A = Q from TMEM (16 dims = 8 packed columns per
+            // step), B = K tile, K-major with 128-byte swizzle.  The
+            // descriptor's start-address field (bytes / 16) is advanced by
+            // addition: one 64-dim box is CHUNK_BYTES / 16, one 16-dim step 2.
+            const uint64_t d0 =
+                tc::smem_desc(stage_base + st * STAGE_BYTES, 16, 1024, tc::kLayoutSw128);
+#pragma unroll 1
+            for (int c = 0; c < nch; ++c) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const int ks = c * 4 + kk;
+                tc::mma_ts(tmem + S_COL, tmem + Q_COL + ks * 8,
+                           d0 + static_cast<uint64_t>(c * (CHUNK_BYTES >> 4) + kk * 2), idS,
+                           ks > 0 ? 1u : 0u);
+              }
+            }
+            tc::commit(s_full);
+          }
+          __syncwarp();
+          ++ns;
+          progress = true;
         }
-        __syncwarp();
-        ++ns;
-        progress = true;
-      }
-      if (progress) {
-        t_idle = 0;
-        spins = 0;
-      } else if ((++spins & 1023u) == 0) {
-        // bounded: give up when nothing became ready for the wait limit
-        // (the timer is read every 1024 idle polls; it is slow to read)
-        const uint64_t now = globaltimer();
-        if (t_idle == 0) {
-          t_idle = now;
-        } else if (now - t_idle > kWaitTimeoutNs) {
-          ok = false;
-          break;
+        if (progress) {
+          t_idle = 0;
+          spins = 0;
+        } else if ((++spins & 1023u) == 0) {
+          // bounded: give up when nothing became ready for the wait limit
+          // (the timer is read every 1024 idle polls; it is slow to read)
+          const uint64_t now = globaltimer();
+          if (t_idle == 0) {
+            t_idle = now;
+          } else if (now - t_idle > kWaitTimeoutNs) {
+            ok = false;
+            return false;
+          }
         }
       }
-    }
+      return true;
+    });
     if (!ok && lane == 0 && p.err_count) atomicAdd(p.err_count, kTimeoutErr);
     if (lane == 0) tc::commit(mma_done);
     __syncwarp();
     warp_wait(mma_done, 0);  // nothing of ours still runs on the tensor core
-  } else if (warp < 4) {
+  } else if (warp != mma_warp && warp != prod_warp) {
     // ------------------------------------------------------------ softmax
-    const int row_i = threadIdx.x;  // TMEM lane / query vector
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const bool own = static_cast<uint32_t>(row_i >> 6) == rank;  // this CTA's softmax rows
+    // Thread = TMEM lane = query vector row_i.  The vectors the peer owns are
+    // forwarded by the two warps of their lane quarters; the vectors this CTA
+    // owns get two warps per lane quarter, one per half of the 64 tokens
+    // (h), which share the row maximum and sum through shared memory.
+    const int quad = warp & 3;
+    const int row_i = quad * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const bool own = static_cast<uint32_t>(row_i >> 6) == rank;
+    const int h = warp >> 2;        // token half (own rows); 0 on forwarding warps
     const int xi = row_i & 63;      // row within the 64-vector exchange blocks
-    const bool lead = xi == 0;      // registers the expected bytes of each message
+    const bool lead = xi == 0 && h == 0;  // registers the expected bytes of each message
     const float scale_log2 = p.sm_scale * kLog2e;
     const uint8_t* xin = smem + OFF_XIN;
     const uint8_t* pin = smem + OFF_PIN;
+    float* red = reinterpret_cast<float*>(smem + OFF_RED);  // [2 tiles][2 halves][64]
+    float* lred = red + 2 * 2 * 64;                          // [2 halves][64]
     // The peer's buffers and barriers (messages are st.async stores that
     // complete their bytes on the receiving CTA's barrier).
     const uint32_t xin_peer = tc::map_peer(smem_u32(smem + OFF_XIN), peer);
@@ -431,18 +521,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     const uint32_t xin_bar_peer0 = tc::map_peer(smem_u32(&xin_full[0]), peer);
     const uint32_t pin_bar_peer0 = tc::map_peer(smem_u32(&pin_full[0]), peer);
     const uint32_t fin_bar_peer = tc::map_peer(smem_u32(fin_full), peer);
-    float m_used = -INFINITY, l_run = 0.f;
     bool ok = true;
+    uint32_t own_phase = 0;
+    // Barrier of the four warps of this CTA's own rows (bounded wait).
+    auto own_sync = [&]() -> bool {
+      mbar_arrive(own_bar);
+      const bool r = warp_wait(own_bar, own_phase & 1);
+      ++own_phase;
+      return r;
+    };
+    // This thread's O columns: all 256 on forwarding rows, half on own rows.
+    const int o_c0 = own ? 128 * h : 0, o_c1 = own ? 128 * h + 128 : 256;
 
-    // Rescales this thread's O row (256 fp32 columns) by alpha once the
-    // previous P.V has completed; warp-uniform (lanes with alpha = 1 keep
-    // their values).
-    auto rescale_o = [&](int n, float alpha) -> bool {
-      if (!__any_sync(0xffffffffu, alpha != 1.f) || n == 0) return true;
+    // Rescales this thread's O columns by alpha once the previous P.V has
+    // completed; warp-uniform (lanes with alpha = 1 keep their values).  Not
+    // needed on a segment's first tile (O is empty).
+    auto rescale_o = [&](int n, int n0, float alpha) -> bool {
+      if (n == n0 || !__any_sync(0xffffffffu, alpha != 1.f)) return true;
       if (!warp_wait(pv_done, (n - 1) & 1)) return false;
       tc::fence_after_sync();
 #pragma unroll 1
-      for (int c = 0; c < 256; c += 32) {
+      for (int c = o_c0; c < o_c1; c += 32) {
         uint32_t o[32];
         tc::ld_32x32b_x32(tmem + lane_base + c, o);
         tc::wait_ld();
@@ -453,180 +552,241 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       tc::wait_st();
       return true;
     };
-    // Stores P into TMEM once the previous P.V has released the columns.
-    auto store_p = [&](int n, const uint32_t (&pk)[32]) -> bool {
-      if (n >= 1 && !warp_wait(pv_done, (n - 1) & 1)) return false;
-      tc::fence_after_sync();
-      tc::st_32x32b_x32(tmem + lane_base + P_COL, pk);
+    auto p_ready = [&]() {
       tc::wait_st();
       tc::fence_before_sync();
       mbar_arrive(p_full);
-      return true;
     };
-    // Loads S_n into sr once the MMA has produced it and frees its columns.
-    auto load_s = [&](int n, uint32_t (&sr)[64]) -> bool {
-      if (!warp_wait(s_full, n & 1)) return false;
-      tc::fence_after_sync();
-      tc::ld_32x32b_x32(tmem + lane_base + S_COL, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tc::ld_32x32b_x32(tmem + lane_base + S_COL + 32,
-                        *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+    auto s_done = [&]() {
       tc::wait_ld();
       tc::fence_before_sync();
       mbar_arrive(s_free);
-      return true;
     };
 
-    if (!own) {
-      // Forwarding rows.  Each warp stores the P of tile np as soon as it
-      // has come back (first: it gates the P.V that frees a KV stage) and
-      // sends its rows' partial scores of tile ns as soon as S is there.
-      // Partial ns goes into the peer's buffer ns & 1, which the peer has
-      // read once it returned the P of tile ns - 2: hence ns <= np + 1.
-      int ns = 0, np = 0;
-      uint64_t t_idle = 0;
-      uint32_t spins = 0;
-      while (np < ntiles) {
-        bool did = false;
-        if (np < ns &&
-            __shfl_sync(0xffffffffu, tc::mbar_test_cluster(&pin_full[np & 1], (np >> 1) & 1),
-                        0)) {
-          const uint8_t* src = pin + (np & 1) * XP_BYTES;
-          uint32_t pk[32];
+    for_each_seg([&](const TcSeg& sg, int k, int n0) -> bool {
+      const int n1 = n0 + cdiv(sg.end - sg.start, TBN);
+      const int v = sg.g * 128 + row_i;
+      const bool valid_v = v < nvec;
+      const int row = valid_v ? sg.b * p.rows_per_seq + v / H : 0;
+      const int hd = valid_v ? v % H : 0;
+      // ---- Q: this thread's vector, dims [64*c0, 64*(c0+nch)), into TMEM
+      // lane row_i as packed bf16 pairs (padding vectors are zeros); on own
+      // rows the two warps take half of the chunks each.  The previous
+      // segment's S products, which read Q, are complete: this thread has
+      // loaded all of them.
+      {
+        const int half = (nch + 1) / 2;
+        const int q_lo = own ? h * half : 0, q_hi = own ? (h ? nch : half) : nch;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            valid_v ? p.q + row * p.q_row_stride + hd * p.q_head_stride + c0 * 64 : p.q);
+        uint32_t r[2][32];
+        auto load_chunk = [&](int c, uint32_t (&d)[32]) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const uint4 x = *reinterpret_cast<const uint4*>(src + xoff(xi, j, XP_ROW));
-            pk[4 * j] = x.x;
-            pk[4 * j + 1] = x.y;
-            pk[4 * j + 2] = x.z;
-            pk[4 * j + 3] = x.w;
+            const uint4 x = valid_v ? __ldg(src + c * 8 + j) : make_uint4(0, 0, 0, 0);
+            d[4 * j] = x.x;
+            d[4 * j + 1] = x.y;
+            d[4 * j + 2] = x.z;
+            d[4 * j + 3] = x.w;
           }
-          const float alpha = reinterpret_cast<const float*>(src + XP_ALPHA)[xi];
-          if (!rescale_o(np, alpha)) { ok = false; break; }
-          if (!store_p(np, pk)) { ok = false; break; }
-          ++np;
-          did = true;
-        }
-        if (ns < ntiles && ns <= np + 1 &&
-            __shfl_sync(0xffffffffu, mbar_test(s_full, ns & 1), 0)) {
-          uint32_t sr[64];
-          if (!load_s(ns, sr)) { ok = false; break; }
-          const int bb = ns & 1;
-          if (lead) mbar_arrive_expect_tx(&pin_full[bb], XP_BYTES);  // P of tile ns
-          const uint32_t dst = xin_peer + bb * XS_BYTES;
-          const uint32_t bar = xin_bar_peer0 + bb * 8;
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            tc::st_async_v4u(dst + xoff(xi, j, XS_ROW), sr[4 * j], sr[4 * j + 1], sr[4 * j + 2],
-                             sr[4 * j + 3], bar);
-          ++ns;
-          did = true;
-        }
-        if (did) {
-          t_idle = 0;
-          spins = 0;
-        } else if ((++spins & 1023u) == 0) {
-          const uint64_t now = globaltimer();
-          if (t_idle == 0) {
-            t_idle = now;
-          } else if (now - t_idle > kWaitTimeoutNs) {
-            ok = false;
-            break;
-          }
-        }
-      }
-    } else {
-      for (int n = 0; n < ntiles && ok; ++n) {
-        const int bb = n & 1;              // exchange buffer
-        const uint32_t u = (n >> 1) & 1;   // its phase parity
-        uint32_t sr[64];
-        if (!load_s(n, sr)) { ok = false; break; }
-        // ---- add the peer's partial scores for this row (xin[bb] is not
-        // rewritten before the peer has received this tile's P)
-        if (lead) mbar_arrive_expect_tx(&xin_full[bb], XS_BYTES);
-        if (!warp_wait_cluster(&xin_full[bb], u)) { ok = false; break; }
-        const uint8_t* src = xin + bb * XS_BYTES;
-        const int valid = min(TBN, end - (start + n * TBN));
-        float mt = -INFINITY;
-#pragma unroll
-        for (int j4 = 0; j4 < 16; ++j4) {
-          const float4 t = *reinterpret_cast<const float4*>(src + xoff(xi, j4, XS_ROW));
-          const float tv[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = 4 * j4 + e;
-            const float s = __uint_as_float(sr[j]) + tv[e];
-            const float x = j < valid ? s * scale_log2 : -INFINITY;
-            sr[j] = __float_as_uint(x);
-            mt = fmaxf(mt, x);
-          }
-        }
-        // ---- online softmax with lazy rescaling
-        const float m_new = fmaxf(m_used, mt);
-        float alpha = 1.f;
-        if (m_new > m_used + kRescaleThreshold) {
-          alpha = n > 0 ? ex2(m_used - m_new) : 1.f;
-          l_run *= alpha;
-          m_used = m_new;
-        }
-        uint32_t pk[32];
-        float psum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float a0 = ex2(__uint_as_float(sr[2 * j]) - m_used);
-          const float a1 = ex2(__uint_as_float(sr[2 * j + 1]) - m_used);
-          psum[j & 3] += a0 + a1;
-          pk[j] = pack_bf16x2(a0, a1);
-        }
-        l_run += (psum[0] + psum[1]) + (psum[2] + psum[3]);
-        // ---- P and alpha to the peer, for its half of O (its buffer bb
-        // held the P of tile n - 2, which it has stored: it sent this
-        // tile's partial scores only afterwards)
-        {
-          const uint32_t dst = pin_peer + bb * XP_BYTES;
-          const uint32_t bar = pin_bar_peer0 + bb * 8;
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            tc::st_async_v4u(dst + xoff(xi, j, XP_ROW), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
-                             pk[4 * j + 3], bar);
-          tc::st_async_b32(dst + XP_ALPHA + 4 * xi, __float_as_uint(alpha), bar);
-        }
-        if (!rescale_o(n, alpha)) { ok = false; break; }
-        if (!store_p(n, pk)) { ok = false; break; }
-      }
-    }
-
-    // ---- the owner's 1 / l reaches the other CTA as a last message
-    float inv = 0.f;
-    if (ok) {
-      if (own) {
-        inv = 1.f / l_run;
-        tc::st_async_b32(fin_peer + 4 * xi, __float_as_uint(inv), fin_bar_peer);
-      } else {
-        if (lead) mbar_arrive_expect_tx(fin_full, 64 * 4);
-        if (warp_wait_cluster(fin_full, 0))
-          inv = reinterpret_cast<const float*>(smem + OFF_FIN)[xi];
-        else
-          ok = false;
-      }
-    }
-    if (!ok) {
-      if (lane == 0 && p.err_count) atomicAdd(p.err_count, kTimeoutErr);
-    } else if (warp_wait(pv_done, (ntiles - 1) & 1)) {
-      tc::fence_after_sync();
-      const int v = v0 + row_i;
-      const bool valid_v = v < nvec;
-      const int row = valid_v ? b * p.rows_per_seq + v / H : 0;
-      const int h = valid_v ? v % H : 0;
-      const int64_t rec = (static_cast<int64_t>(row) * S + s0) * H + h;
+        };
+        // the loads of chunk c + 1 are issued before chunk c goes to TMEM
+        load_chunk(q_lo, r[0]);
 #pragma unroll 1
-      for (int c = 0; c < 256; c += 32) {
+        for (int c = q_lo; c < q_hi; c += 2) {
+          if (c + 1 < q_hi) load_chunk(c + 1, r[1]);
+          tc::st_32x32b_x32(tmem + lane_base + Q_COL + c * 32, r[0]);
+          if (c + 1 < q_hi) {
+            if (c + 2 < q_hi) load_chunk(c + 2, r[0]);
+            tc::st_32x32b_x32(tmem + lane_base + Q_COL + (c + 1) * 32, r[1]);
+          }
+        }
+        tc::wait_st();
+        tc::fence_before_sync();
+        mbar_arrive(q_ready);
+      }
+      float m_used = -INFINITY, l_run = 0.f;
+
+      if (!own) {
+        // Forwarding rows.  Each warp stores the P of tile np as soon as it
+        // has come back (first: it gates the P.V that frees a KV stage) and
+        // sends its rows' partial scores of tile ns as soon as S is there.
+        // Partial ns goes into the peer's buffer ns & 1, which the peer has
+        // read once it returned the P of tile ns - 2: hence ns <= np + 1.
+        int ns = n0, np = n0;
+        uint64_t t_idle = 0;
+        uint32_t spins = 0;
+        while (np < n1) {
+          bool did = false;
+          if (np < ns &&
+              __shfl_sync(0xffffffffu, tc::mbar_test_cluster(&pin_full[np & 1], (np >> 1) & 1),
+                          0)) {
+            const uint8_t* src = pin + (np & 1) * XP_BYTES;
+            uint32_t pk[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint4 x = *reinterpret_cast<const uint4*>(src + xoff(xi, j, XP_ROW));
+              pk[4 * j] = x.x;
+              pk[4 * j + 1] = x.y;
+              pk[4 * j + 2] = x.z;
+              pk[4 * j + 3] = x.w;
+            }
+            const float alpha = reinterpret_cast<const float*>(src + XP_ALPHA)[xi];
+            if (!rescale_o(np, n0, alpha)) { ok = false; break; }
+            // P's columns are free once the previous P.V has completed
+            if (np >= 1 && !warp_wait(pv_done, (np - 1) & 1)) { ok = false; break; }
+            tc::fence_after_sync();
+            tc::st_32x32b_x32(tmem + lane_base + P_COL, pk);
+            p_ready();
+            ++np;
+            did = true;
+          }
+          if (ns < n1 && ns <= np + 1 &&
+              __shfl_sync(0xffffffffu, mbar_test(s_full, ns & 1), 0)) {
+            tc::fence_after_sync();
+            uint32_t sr[64];
+            tc::ld_32x32b_x32(tmem + lane_base + S_COL,
+                              *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tc::ld_32x32b_x32(tmem + lane_base + S_COL + 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            s_done();
+            const int bb = ns & 1;
+            if (lead) mbar_arrive_expect_tx(&pin_full[bb], XP_BYTES);  // P of tile ns
+            const uint32_t dst = xin_peer + bb * XS_BYTES;
+            const uint32_t bar = xin_bar_peer0 + bb * 8;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              tc::st_async_v4u(dst + xoff(xi, j, XS_ROW), sr[4 * j], sr[4 * j + 1],
+                               sr[4 * j + 2], sr[4 * j + 3], bar);
+            ++ns;
+            did = true;
+          }
+          if (did) {
+            t_idle = 0;
+            spins = 0;
+          } else if ((++spins & 1023u) == 0) {
+            const uint64_t now = globaltimer();
+            if (t_idle == 0) {
+              t_idle = now;
+            } else if (now - t_idle > kWaitTimeoutNs) {
+              ok = false;
+              break;
+            }
+          }
+        }
+      } else {
+        for (int n = n0; n < n1 && ok; ++n) {
+          const int bb = n & 1;              // exchange buffer
+          const uint32_t u = (n >> 1) & 1;   // its phase parity
+          // ---- this half's 32 partial scores
+          if (!warp_wait(s_full, n & 1)) { ok = false; break; }
+          tc::fence_after_sync();
+          uint32_t sr[32];
+          tc::ld_32x32b_x32(tmem + lane_base + S_COL + 32 * h, sr);
+          s_done();
+          // ---- add the peer's partial scores for them (xin[bb] is not
+          // rewritten before the peer has received this tile's P)
+          if (lead) mbar_arrive_expect_tx(&xin_full[bb], XS_BYTES);
+          if (!warp_wait_cluster(&xin_full[bb], u)) { ok = false; break; }
+          const uint8_t* src = xin + bb * XS_BYTES;
+          const int valid = min(TBN, sg.end - (sg.start + (n - n0) * TBN)) - 32 * h;
+          float mt = -INFINITY;
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 t =
+                *reinterpret_cast<const float4*>(src + xoff(xi, 8 * h + j4, XS_ROW));
+            const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = 4 * j4 + e;
+              const float s = __uint_as_float(sr[j]) + tv[e];
+              const float x = j < valid ? s * scale_log2 : -INFINITY;
+              sr[j] = __float_as_uint(x);
+              mt = fmaxf(mt, x);
+            }
+          }
+          // ---- row maximum over both halves (buffer by tile parity: the
+          // other half reads this tile's value before either writes the
+          // tile after next's)
+          red[(bb * 2 + h) * 64 + xi] = mt;
+          if (!own_sync()) { ok = false; break; }
+          mt = fmaxf(red[(bb * 2) * 64 + xi], red[(bb * 2 + 1) * 64 + xi]);
+          // ---- online softmax with lazy rescaling (both halves take the
+          // same decision from the same values)
+          const float m_new = fmaxf(m_used, mt);
+          float alpha = 1.f;
+          if (m_new > m_used + kRescaleThreshold) {
+            alpha = n > n0 ? ex2(m_used - m_new) : 1.f;
+            l_run *= alpha;
+            m_used = m_new;
+          }
+          uint32_t pk[16];
+          float psum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float a0 = ex2(__uint_as_float(sr[2 * j]) - m_used);
+            const float a1 = ex2(__uint_as_float(sr[2 * j + 1]) - m_used);
+            psum[j & 3] += a0 + a1;
+            pk[j] = pack_bf16x2(a0, a1);
+          }
+          l_run += (psum[0] + psum[1]) + (psum[2] + psum[3]);
+          // ---- this half of P, and alpha, to the peer for its half of O
+          // (its buffer bb held the P of tile n - 2, which it has stored: it
+          // sent this tile's partial scores only afterwards)
+          {
+            const uint32_t dst = pin_peer + bb * XP_BYTES;
+            const uint32_t bar = pin_bar_peer0 + bb * 8;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tc::st_async_v4u(dst + xoff(xi, 4 * h + j, XP_ROW), pk[4 * j], pk[4 * j + 1],
+                               pk[4 * j + 2], pk[4 * j + 3], bar);
+            if (h == 0) tc::st_async_b32(dst + XP_ALPHA + 4 * xi, __float_as_uint(alpha), bar);
+          }
+          if (!rescale_o(n, n0, alpha)) { ok = false; break; }
+          if (n >= 1 && !warp_wait(pv_done, (n - 1) & 1)) { ok = false; break; }
+          tc::fence_after_sync();
+          tc::st_32x32b_x16(tmem + lane_base + P_COL + 16 * h, pk);
+          p_ready();
+        }
+        // ---- row sum over both halves
+        if (ok) {
+          lred[h * 64 + xi] = l_run;
+          if (!own_sync()) ok = false;
+          l_run = lred[xi] + lred[64 + xi];
+        }
+      }
+
+      // ---- the owner's 1 / l reaches the other CTA as the segment's last
+      // message (the peer read the previous segment's before it sent any
+      // partial scores of this one)
+      float inv = 0.f;
+      if (ok) {
+        if (own) {
+          inv = 1.f / l_run;
+          if (h == 0) tc::st_async_b32(fin_peer + 4 * xi, __float_as_uint(inv), fin_bar_peer);
+        } else {
+          if (lead) mbar_arrive_expect_tx(fin_full, 64 * 4);
+          if (warp_wait_cluster(fin_full, k & 1))
+            inv = reinterpret_cast<const float*>(smem + OFF_FIN)[xi];
+          else
+            ok = false;
+        }
+      }
+      if (!ok) return false;
+      // ---- epilogue: this thread's O columns (normalised) and, from the
+      // owner, lse
+      if (!warp_wait(pv_done, (n1 - 1) & 1)) { ok = false; return false; }
+      tc::fence_after_sync();
+      const int64_t rec = (static_cast<int64_t>(row) * S + sg.slot) * H + hd;
+#pragma unroll 1
+      for (int c = o_c0; c < o_c1; c += 32) {
         uint32_t o[32];
         tc::ld_32x32b_x32(tmem + lane_base + c, o);
         tc::wait_ld();
         if (!valid_v) continue;
         const int col = rank * 256 + c;
-        if (S == 1) {
-          uint16_t* dst = p.o + (static_cast<int64_t>(row) * H + h) * 512 + col;
+        if (sg.direct) {
+          uint16_t* dst = p.o + (static_cast<int64_t>(row) * H + hd) * 512 + col;
 #pragma unroll
           for (int j = 0; j < 32; j += 8)
             *reinterpret_cast<uint4*>(dst + j) = make_uint4(
@@ -643,22 +803,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
                             __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
         }
       }
-      if (valid_v && own) {
+      tc::fence_before_sync();
+      mbar_arrive(o_free);
+      if (valid_v && own && h == 0) {
         float lg;
         asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(l_run));
         const float lse = (m_used + lg) * kLn2;
-        if (S == 1) {
-          p.lse[static_cast<int64_t>(row) * H + h] = lse;
+        if (sg.direct) {
+          p.lse[static_cast<int64_t>(row) * H + hd] = lse;
         } else {
           p.ws_lse[rec] = lse;
-          // splits fused into this CTA pair hold no partial of their own
-          for (int s = s0 + 1; s < s1; ++s)
-            p.ws_lse[(static_cast<int64_t>(row) * S + s) * H + h] = -INFINITY;
+          for (int s = sg.mark_lo; s < sg.mark_hi; ++s)
+            p.ws_lse[(static_cast<int64_t>(row) * S + s) * H + hd] = -INFINITY;
         }
       }
-    } else if (lane == 0 && p.err_count) {
-      atomicAdd(p.err_count, kTimeoutErr);
-    }
+      return true;
+    });
+    if (!ok && lane == 0 && p.err_count) atomicAdd(p.err_count, kTimeoutErr);
   }
 
   // ---------------------------------------------------------------- teardown
@@ -700,7 +861,7 @@ int tc_split_group(const DecodeParams& p, int sm_count) {
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, const CUtensorMap& tmap,
-                             int split_group, cudaStream_t stream) {
+                             int split_group, int sm_count, cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(
@@ -709,10 +870,17 @@ cudaError_t launch_decode_tc(const DecodeParams& p, const CUtensorMap& tmap,
     attr_done = true;
   }
   const int qblocks = (p.rows_per_seq * p.num_heads + 127) / 128;
+  const int64_t units = static_cast<int64_t>(qblocks) * p.num_seqs;
+  if (p.num_splits > 1 && units <= kMaxPersistUnits) {
+    // persistent: one CTA pair per two SMs, tiles balanced over the pairs
+    const int pairs = sm_count >= 2 ? sm_count / 2 : 1;
+    return launch_overlapped(decode_tc_kernel, dim3(2 * pairs), dim3(TC_THREADS), TC_SMEM,
+                             stream, p, tmap, split_group, 1);
+  }
   const int groups = (p.num_splits + split_group - 1) / split_group;
   const dim3 grid(2 * qblocks, groups, p.num_seqs);
   return launch_overlapped(decode_tc_kernel, grid, dim3(TC_THREADS), TC_SMEM, stream, p, tmap,
-                           split_group);
+                           split_group, 0);
 }
 
 }  // namespace mla

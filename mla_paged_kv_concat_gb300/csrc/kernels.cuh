@@ -72,11 +72,15 @@ cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap,
                               const CUtensorMap& qmap, int R, bool fp8, int sm_count,
                               cudaStream_t stream);
 
-// Stage 1 on tcgen05/TMEM for bf16 caches with R = 512: one 2-CTA cluster per
-// 128 query vectors and group of `split_group` consecutive splits.  `tmap` as
-// above ({64, min(block_size, 64), 1} box, 128-byte swizzle).
+// Stage 1 on tcgen05/TMEM for bf16 caches with R = 512, 2-CTA clusters of 128
+// query vectors.  With num_kv_splits > 1 (and at most kMaxPersistUnits
+// (sequence, 128-vector block) units) it runs persistent, sm_count / 2 pairs
+// with the tiles balanced over them; otherwise one pair per 128 vectors and
+// group of `split_group` consecutive splits.  `tmap` as above ({64,
+// min(block_size, 64), 1} box, 128-byte swizzle).  Launched overlapped with
+// the previous kernel of the stream.
 cudaError_t launch_decode_tc(const DecodeParams& p, const CUtensorMap& tmap,
-                             int split_group, cudaStream_t stream);
+                             int split_group, int sm_count, cudaStream_t stream);
 // Consecutive splits the tcgen05 kernel processes per CTA pair.
 int tc_split_group(const DecodeParams& p, int sm_count);
 

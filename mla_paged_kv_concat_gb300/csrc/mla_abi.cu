@@ -303,7 +303,8 @@ mla_status run_stage1(const mla::DecodeParams& p_in, const void* kv_cache,
                   ? 1
                   : 0;
   cudaError_t e =
-      tc ? mla::launch_decode_tc(p, tmap, mla::tc_split_group(p, device_sm_count()), s)
+      tc ? mla::launch_decode_tc(p, tmap, mla::tc_split_group(p, device_sm_count()),
+                                  device_sm_count(), s)
          : mla::launch_decode_mma(p, tmap, qmap, R, fp8, device_sm_count(), s);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
