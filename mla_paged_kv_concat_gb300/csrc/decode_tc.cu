@@ -258,10 +258,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     }
     nseg = 1;
   }
-  // Walks this pair's segments in order, calling f(seg, index, first tile).
+  // Walks this pair's segments in order, calling f(seg, index, first tile
+  // (a running count over the pair's segments), next segment or nullptr).
+  auto make_seg = [&](int u, TcSeg& s) {
+    const int t_lo = max(lo, pre[u]) - pre[u], t_hi = min(hi, pre[u + 1]) - pre[u];
+    s.b = u / qblocks;
+    s.g = u - s.b * qblocks;
+    const int L = lens[s.b] & ~kClampedBit;
+    s.start = t_lo * TBN;
+    s.end = min(L, t_hi * TBN);
+    const int cf = pre[u] / C;
+    s.slot = cidx - cf;
+    s.mark_lo = s.slot == 0 ? (pre[u + 1] - 1) / C - cf + 1 : S;
+    s.mark_hi = S;
+    s.direct = false;
+  };
+  // first unit at or after u that has tiles in [lo, hi), or -1
+  auto next_unit = [&](int u) {
+    for (; u < units && pre[u] < hi; ++u)
+      if (min(hi, pre[u + 1]) > max(lo, pre[u])) return u;
+    return -1;
+  };
   auto for_each_seg = [&](auto&& f) {
     if (!persistent) {
-      if (nseg) f(gseg, 0, 0);
+      if (nseg) f(gseg, 0, 0, static_cast<const TcSeg*>(nullptr));
       return;
     }
     int a = 0, z = units;  // first unit with pre[u + 1] > lo
@@ -269,26 +289,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       const int m = (a + z) >> 1;
       if (pre[m + 1] > lo) z = m; else a = m + 1;
     }
-    int k = 0, n0 = 0;
-    for (int u = a; u < units && pre[u] < hi; ++u) {
-      const int t_lo = max(lo, pre[u]) - pre[u], t_hi = min(hi, pre[u + 1]) - pre[u];
-      if (t_hi <= t_lo) continue;
-      TcSeg s;
-      s.b = u / qblocks;
-      s.g = u - s.b * qblocks;
-      const int L = lens[s.b] & ~kClampedBit;
-      s.start = t_lo * TBN;
-      s.end = min(L, t_hi * TBN);
-      const int cf = pre[u] / C;
-      s.slot = cidx - cf;
-      s.mark_lo = s.slot == 0 ? (pre[u + 1] - 1) / C - cf + 1 : S;
-      s.mark_hi = S;
-      s.direct = false;
-      if (s.slot == 0 && s.g == 0 && (lens[s.b] & kClampedBit) && threadIdx.x == 0 &&
+    int u = next_unit(a);
+    if (u < 0) return;
+    TcSeg cur, nxt;
+    make_seg(u, cur);
+    for (int k = 0, n0 = 0;; ++k) {
+      const int u2 = next_unit(u + 1);
+      if (u2 >= 0) make_seg(u2, nxt);
+      if (cur.slot == 0 && cur.g == 0 && (lens[cur.b] & kClampedBit) && threadIdx.x == 0 &&
           rank == 0 && p.err_count)
         atomicAdd(p.err_count, 1);  // seq_len beyond the block table, once per sequence
-      if (!f(s, k++, n0)) return;
-      n0 += t_hi - t_lo;
+      if (!f(cur, k, n0, u2 >= 0 ? &nxt : static_cast<const TcSeg*>(nullptr))) return;
+      if (u2 < 0) return;
+      n0 += cdiv(cur.end - cur.start, TBN);
+      u = u2;
+      cur = nxt;
     }
   };
 
@@ -332,7 +347,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       const int rows_box = bs < TBN ? bs : TBN;
       const int npg = TBN / rows_box;
       int n = 0;  // tiles issued (ring position)
-      for_each_seg([&](const TcSeg& sg, int, int) -> bool {
+      for_each_seg([&](const TcSeg& sg, int, int, const TcSeg*) -> bool {
         const int32_t* bt = p.block_table + static_cast<int64_t>(sg.b) * p.bt_stride;
         const int ntiles = cdiv(sg.end - sg.start, TBN);
         // Block ids of tile t of the segment (pages past its end read as 0
@@ -396,7 +411,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     // between the CTAs.
     bool ok = true;
     int ns = 0, npv = 0;  // global tile counters
-    for_each_seg([&](const TcSeg& sg, int k, int n0) -> bool {
+    for_each_seg([&](const TcSeg& sg, int k, int n0, const TcSeg*) -> bool {
       const int n1 = n0 + cdiv(sg.end - sg.start, TBN);
       uint64_t t_idle = 0;
       uint32_t spins = 0;
@@ -545,6 +560,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         uint32_t o[32];
         tc::ld_32x32b_x32(tmem + lane_base + c, o);
         tc::wait_ld();
+        tc::reg_fence(o);
 #pragma unroll
         for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
         tc::st_32x32b_x32(tmem + lane_base + c, o);
@@ -563,48 +579,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       mbar_arrive(s_free);
     };
 
-    for_each_seg([&](const TcSeg& sg, int k, int n0) -> bool {
+    // ---- Q of a segment: this thread's vector, dims [64*c0, 64*(c0+nch)),
+    // into TMEM lane row_i as packed bf16 pairs (padding vectors are zeros);
+    // on own rows the two warps take half of the chunks each.  Called once
+    // the previous segment's S products, which read Q, are complete (this
+    // thread has loaded all of them).
+    auto load_q = [&](const TcSeg& sg) {
+      const int v = sg.g * 128 + row_i;
+      const bool valid_v = v < nvec;
+      const int row = valid_v ? sg.b * p.rows_per_seq + v / H : 0;
+      const int hd = valid_v ? v % H : 0;
+      const int half = (nch + 1) / 2;
+      const int q_lo = own ? h * half : 0, q_hi = own ? (h ? nch : half) : nch;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          valid_v ? p.q + row * p.q_row_stride + hd * p.q_head_stride + c0 * 64 : p.q);
+      uint32_t r[2][32];
+      auto load_chunk = [&](int c, uint32_t (&d)[32]) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 x = valid_v ? __ldg(src + c * 8 + j) : make_uint4(0, 0, 0, 0);
+          d[4 * j] = x.x;
+          d[4 * j + 1] = x.y;
+          d[4 * j + 2] = x.z;
+          d[4 * j + 3] = x.w;
+        }
+      };
+      // the loads of chunk c + 1 are issued before chunk c goes to TMEM
+      load_chunk(q_lo, r[0]);
+#pragma unroll 1
+      for (int c = q_lo; c < q_hi; c += 2) {
+        if (c + 1 < q_hi) load_chunk(c + 1, r[1]);
+        tc::st_32x32b_x32(tmem + lane_base + Q_COL + c * 32, r[0]);
+        if (c + 1 < q_hi) {
+          if (c + 2 < q_hi) load_chunk(c + 2, r[0]);
+          tc::st_32x32b_x32(tmem + lane_base + Q_COL + (c + 1) * 32, r[1]);
+        }
+      }
+      tc::wait_st();
+      tc::fence_before_sync();
+      mbar_arrive(q_ready);
+    };
+    // L2 prefetch of a segment's Q lines for this thread (used at its start)
+    auto prefetch_q = [&](const TcSeg& sg) {
+      const int v = sg.g * 128 + row_i;
+      if (v >= nvec) return;
+      const uint16_t* src = p.q + (sg.b * p.rows_per_seq + v / H) * p.q_row_stride +
+                            (v % H) * p.q_head_stride + c0 * 64;
+      for (int c = 0; c < nch; ++c)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + c * 64));
+    };
+
+    for_each_seg([&](const TcSeg& sg, int k, int n0, const TcSeg* next) -> bool {
       const int n1 = n0 + cdiv(sg.end - sg.start, TBN);
       const int v = sg.g * 128 + row_i;
       const bool valid_v = v < nvec;
       const int row = valid_v ? sg.b * p.rows_per_seq + v / H : 0;
       const int hd = valid_v ? v % H : 0;
-      // ---- Q: this thread's vector, dims [64*c0, 64*(c0+nch)), into TMEM
-      // lane row_i as packed bf16 pairs (padding vectors are zeros); on own
-      // rows the two warps take half of the chunks each.  The previous
-      // segment's S products, which read Q, are complete: this thread has
-      // loaded all of them.
-      {
-        const int half = (nch + 1) / 2;
-        const int q_lo = own ? h * half : 0, q_hi = own ? (h ? nch : half) : nch;
-        const uint4* src = reinterpret_cast<const uint4*>(
-            valid_v ? p.q + row * p.q_row_stride + hd * p.q_head_stride + c0 * 64 : p.q);
-        uint32_t r[2][32];
-        auto load_chunk = [&](int c, uint32_t (&d)[32]) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 x = valid_v ? __ldg(src + c * 8 + j) : make_uint4(0, 0, 0, 0);
-            d[4 * j] = x.x;
-            d[4 * j + 1] = x.y;
-            d[4 * j + 2] = x.z;
-            d[4 * j + 3] = x.w;
-          }
-        };
-        // the loads of chunk c + 1 are issued before chunk c goes to TMEM
-        load_chunk(q_lo, r[0]);
-#pragma unroll 1
-        for (int c = q_lo; c < q_hi; c += 2) {
-          if (c + 1 < q_hi) load_chunk(c + 1, r[1]);
-          tc::st_32x32b_x32(tmem + lane_base + Q_COL + c * 32, r[0]);
-          if (c + 1 < q_hi) {
-            if (c + 2 < q_hi) load_chunk(c + 2, r[0]);
-            tc::st_32x32b_x32(tmem + lane_base + Q_COL + (c + 1) * 32, r[1]);
-          }
-        }
-        tc::wait_st();
-        tc::fence_before_sync();
-        mbar_arrive(q_ready);
-      }
+      if (k == 0) load_q(sg);  // later segments' Q is loaded at the end of the previous one
+      if (next) prefetch_q(*next);
       float m_used = -INFINITY, l_run = 0.f;
 
       if (!own) {
@@ -650,6 +682,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             tc::ld_32x32b_x32(tmem + lane_base + S_COL + 32,
                               *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
             s_done();
+            tc::reg_fence(sr);
             const int bb = ns & 1;
             if (lead) mbar_arrive_expect_tx(&pin_full[bb], XP_BYTES);  // P of tile ns
             const uint32_t dst = xin_peer + bb * XS_BYTES;
@@ -684,6 +717,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           uint32_t sr[32];
           tc::ld_32x32b_x32(tmem + lane_base + S_COL + 32 * h, sr);
           s_done();
+          tc::reg_fence(sr);
           // ---- add the peer's partial scores for them (xin[bb] is not
           // rewritten before the peer has received this tile's P)
           if (lead) mbar_arrive_expect_tx(&xin_full[bb], XS_BYTES);
@@ -773,17 +807,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         }
       }
       if (!ok) return false;
+      // ---- the next segment's Q first, so that its S products start while
+      // this segment's O is read out
+      if (next) load_q(*next);
       // ---- epilogue: this thread's O columns (normalised) and, from the
       // owner, lse
       if (!warp_wait(pv_done, (n1 - 1) & 1)) { ok = false; return false; }
       tc::fence_after_sync();
       const int64_t rec = (static_cast<int64_t>(row) * S + sg.slot) * H + hd;
-#pragma unroll 1
-      for (int c = o_c0; c < o_c1; c += 32) {
-        uint32_t o[32];
-        tc::ld_32x32b_x32(tmem + lane_base + c, o);
-        tc::wait_ld();
-        if (!valid_v) continue;
+      // two TMEM loads in flight: columns c + 32 come in while c is stored
+      auto store_cols = [&](int c, const uint32_t (&o)[32]) {
+        if (!valid_v) return;
         const int col = rank * 256 + c;
         if (sg.direct) {
           uint16_t* dst = p.o + (static_cast<int64_t>(row) * H + hd) * 512 + col;
@@ -802,6 +836,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
                 make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
                             __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
         }
+      };
+      uint32_t oa[32], ob[32];
+      tc::ld_32x32b_x32(tmem + lane_base + o_c0, oa);
+#pragma unroll 1
+      for (int c = o_c0; c < o_c1; c += 64) {
+        tc::wait_ld();
+        tc::reg_fence(oa);
+        tc::ld_32x32b_x32(tmem + lane_base + c + 32, ob);  // o_c1 - o_c0 is a multiple of 64
+        store_cols(c, oa);
+        tc::wait_ld();
+        tc::reg_fence(ob);
+        if (c + 64 < o_c1) tc::ld_32x32b_x32(tmem + lane_base + c + 64, oa);
+        store_cols(c + 32, ob);
       }
       tc::fence_before_sync();
       mbar_arrive(o_free);

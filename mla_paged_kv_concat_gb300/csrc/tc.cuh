@@ -141,6 +141,13 @@ __device__ __forceinline__ void st_32x32b_x16(uint32_t taddr, const uint32_t (&r
 __device__ __forceinline__ void wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// Ties registers written by tcgen05.ld to the preceding wait_ld(): code
+// that reads them cannot be scheduled above this point.
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
 __device__ __forceinline__ void wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
