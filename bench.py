@@ -193,6 +193,20 @@ def run_ours(args, rank, world, local_rank):
     launches_per_step = (1 if T else 0) + 1 + (1 if S > 1 else 0)
 
     def step_events():
+        # One step bracketed by two events only: an event recorded between
+        # two kernels would stop the next one from launching while the
+        # previous one drains (programmatic dependent launch).
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e[0].record(stream)
+        write(kv_c, k_pe, slots)
+        stage1(q, bt, sl, o, lse)
+        merge(sl, o, lse)
+        e[1].record(stream)
+        return e
+
+    def step_kernel_events():
+        # The same step with an event between the kernels, for the per-kernel
+        # times (the stage-1 time is the roofline's denominator).
         e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         e[0].record(stream)
         write(kv_c, k_pe, slots)
@@ -214,9 +228,11 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(args.warmup):
         flush_l2()
         step_events()
+        flush_l2()
+        step_kernel_events()
     torch.cuda.synchronize(dev)
 
-    evs = []
+    evs, kevs = [], []
     with ClockSampler(local_rank) as clk:
         barrier()
         torch.cuda.synchronize(dev)
@@ -225,10 +241,14 @@ def run_ours(args, rank, world, local_rank):
             evs.append(step_events())
         torch.cuda.synchronize(dev)
         barrier()
-    t_write = [e[0].elapsed_time(e[1]) for e in evs]
-    t_s1 = [e[1].elapsed_time(e[2]) for e in evs]
-    t_merge = [e[2].elapsed_time(e[3]) for e in evs]
-    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+        for _ in range(args.steps):
+            flush_l2()
+            kevs.append(step_kernel_events())
+        torch.cuda.synchronize(dev)
+    t_write = [e[0].elapsed_time(e[1]) for e in kevs]
+    t_s1 = [e[1].elapsed_time(e[2]) for e in kevs]
+    t_merge = [e[2].elapsed_time(e[3]) for e in kevs]
+    t_step = [e[0].elapsed_time(e[1]) for e in evs]
     total_ms = float(np.sum(t_step))
     if dist is not None:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
@@ -294,8 +314,13 @@ def run_ours(args, rank, world, local_rank):
     hbm, bf16, src = _peaks()
     s1_ms = float(np.mean(t_s1))
     achieved = kv_bytes / (s1_ms * 1e-3) / 1e9
+    # the stage-1 kernel the library picks (tcgen05 for bf16, R = 512 and at
+    # least 128 query vectors per sequence; warp MMA otherwise)
+    tc = (not w.kv_fp8) and R == 512 and w.rows_per_seq * H >= 128 and args.path != 1
+    tc = tc or args.path == 2
+    kernel_src = "decode_tc.cu" if tc else "decode_mma.cu"
     traffic = _traffic_record(os.path.join(ROOT, "mla_paged_kv_concat_gb300", "csrc",
-                                           "decode_mma.cu"), args.workload)
+                                           kernel_src), args.workload)
     roof_t = max(kv_bytes / (hbm * 1e9), flops / (bf16 * 1e12))
     line = {
         "metric": "MLA decode KV GB/s & TFLOPS as % of roofline; decode rows/s at 1 GB300",
@@ -323,7 +348,8 @@ def run_ours(args, rank, world, local_rank):
         "kernel_ms": {"cache_write": round(float(np.mean(t_write)), 5),
                       "decode_splitkv": round(s1_ms, 5),
                       "decode_merge": round(float(np.mean(t_merge)), 5)},
-        "roofline": {"bound": "hbm", "kernel": "decode_splitkv (stage 1)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("decode_tc_kernel" if tc else "decode_mma_kernel") + " (stage 1)",
                      "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": traffic,
                      "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs, burst)"},
