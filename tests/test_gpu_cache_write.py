@@ -125,3 +125,32 @@ def test_num_tokens_smaller_than_rows(cuda_dev):
     d.write()
     torch.cuda.synchronize()
     assert d.cache_numpy().tobytes() == oracle_cache(w).tobytes()
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.05, 0.3, 7.0, 1e-30, 3e37])
+def test_fp8_every_bf16_value(cuda_dev, scale):
+    """Every finite bf16 bit pattern through the fp8 write, byte-exact against
+    the oracle's IEEE division and E4M3 rounding (ties, subnormals, saturation,
+    and quotients next to a rounding boundary, where the kernel falls back to
+    the division)."""
+    R, P = 256, 64
+    D = R + P
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = W.bits_to_torch_bf16(bits).float().numpy()
+    bits = bits[np.isfinite(vals)]
+    T = (bits.size + D - 1) // D
+    pad = np.zeros(T * D - bits.size, np.uint16)
+    rows = np.concatenate([bits, pad]).reshape(T, D)
+    full = W.bits_to_torch_bf16(rows)
+    bs = 64
+    nb = (T + bs - 1) // bs
+    w = W.make_workload("fp8all", seed=54, seq_lens=[1], num_heads=1, kv_lora_rank=R,
+                        pool_blocks=nb, block_size=bs, write="random", num_write_tokens=T)
+    w.kv_c, w.k_pe = full[:, :R], full[:, R:]
+    w.slot_mapping = np.arange(T, dtype=np.int64)
+    w.kv_fp8, w.kv_scale = True, float(np.float32(scale))
+    w.kv_cache = np.zeros((nb, bs, D), np.uint8)
+    d = Dev(w)
+    d.write()
+    torch.cuda.synchronize()
+    assert d.cache_numpy().tobytes() == oracle_cache(w).tobytes()
