@@ -79,6 +79,8 @@ def _load():
         lib.oracle_num_kv_splits.argtypes = [i64, i32, i32]
         lib.oracle_num_kv_splits.restype = i32
         lib.oracle_max_threads.restype = i32
+        lib.oracle_lse_merge.argtypes = [P, P, i32, i64, i32, P, P]
+        lib.oracle_lse_merge.restype = None
         _lib = lib
         return lib
 
@@ -191,4 +193,18 @@ def decode(q, kv_cache: np.ndarray, block_table, seq_lens, *, block_size: int,
         bt.shape[1], _ptr(sl), sl.size, float(sm_scale), float(kv_scale),
         int(num_kv_splits), None if pr is None else _ptr(pr), n, _ptr(o), _ptr(lse),
         _ptr(ss), maxl, _ptr(so), nthr)
+    return o, lse
+
+
+def lse_merge(o_parts, lse_parts):
+    """Cross-shard LSE merge in fp64.  ``o_parts`` [G, n, R], ``lse_parts``
+    [G, n] (any float dtype; -inf marks an empty part).  Returns (o [n, R],
+    lse [n]) float64."""
+    op = np.ascontiguousarray(np.asarray(o_parts, dtype=np.float64))
+    lp = np.ascontiguousarray(np.asarray(lse_parts, dtype=np.float64))
+    G, n, R = op.shape
+    assert lp.shape == (G, n)
+    o = np.empty((n, R), np.float64)
+    lse = np.empty(n, np.float64)
+    _load().oracle_lse_merge(_ptr(op), _ptr(lp), G, n, R, _ptr(o), _ptr(lse))
     return o, lse

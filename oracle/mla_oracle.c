@@ -313,6 +313,41 @@ void oracle_decode(const uint16_t *q, int64_t q_row_stride,
  * split count from max_seq_len / 512, capped at sm_count * 2; [note] Data
  * flow: VLLM_BATCH_INVARIANT forces 1 split).  The body is not printed; the
  * plainest reading is min(ceil(max_seq_len / 512), 2 * sm_count), at least 1. */
+/* Cross-shard merge ([note] Data flow: with decode context parallelism each
+ * rank attends over its shard of the KV tokens and cp_lse_ag_out_rs combines
+ * the (o, lse) pairs; [api] decode with DCP all-gathers q heads first).  The
+ * same LSE algebra as the split merge above: for each of n (row, head)
+ * records, M = max over the G parts of lse_g (parts with lse = -inf hold no
+ * tokens and are skipped), o = sum e^{lse_g - M} o_g / sum e^{lse_g - M},
+ * lse = M + ln sum e^{lse_g - M}, parts visited in index order; when every
+ * part is empty, o = 0 and lse = -inf.  o_parts is [G][n][R], lse_parts
+ * [G][n], both fp64. */
+void oracle_lse_merge(const double *o_parts, const double *lse_parts, int G, int64_t n,
+                      int R, double *o, double *lse) {
+  for (int64_t i = 0; i < n; ++i) {
+    double M = -INFINITY;
+    for (int g = 0; g < G; ++g)
+      if (lse_parts[(int64_t)g * n + i] > M) M = lse_parts[(int64_t)g * n + i];
+    double *oi = o + i * R;
+    for (int d = 0; d < R; ++d) oi[d] = 0.0;
+    if (M == -INFINITY) {
+      lse[i] = -INFINITY;
+      continue;
+    }
+    double den = 0.0;
+    for (int g = 0; g < G; ++g) {
+      double lg = lse_parts[(int64_t)g * n + i];
+      if (lg == -INFINITY) continue;
+      double w = exp(lg - M);
+      const double *og = o_parts + ((int64_t)g * n + i) * R;
+      for (int d = 0; d < R; ++d) oi[d] += w * og[d];
+      den += w;
+    }
+    for (int d = 0; d < R; ++d) oi[d] /= den;
+    lse[i] = M + log(den);
+  }
+}
+
 int oracle_num_kv_splits(int64_t max_seq_len, int sm_count, int deterministic) {
   if (deterministic) return 1;
   int64_t s = (max_seq_len + 511) / 512;
