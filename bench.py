@@ -361,6 +361,68 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+# ---------------------------------------------------------------- cross-shard merge
+def run_lse_merge(args):
+    """Time mla_lse_merge alone: G shards' (o, lse) of a decode batch (rows x
+    H query vectors, R-wide latent) merged into one.  HBM-bound: it reads
+    every part once and writes the result once."""
+    import torch
+    import mla_paged_kv_concat_gb300 as mla
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lib = mla.load()
+    G, rows, H, R = args.parts, args.merge_rows, args.merge_heads, 512
+    n = rows * H
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    o_parts = torch.randn(G, rows, H, R, device=dev, generator=gen).to(torch.bfloat16)
+    lse_parts = torch.randn(G, rows, H, device=dev, generator=gen) * 4.0
+    o = torch.empty(rows, H, R, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(rows, H, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = int(stream.cuda_stream)
+
+    def merge():
+        st = lib.mla_lse_merge(o_parts.data_ptr(), o_parts.stride(0), lse_parts.data_ptr(),
+                               lse_parts.stride(0), G, rows, H, R, o.data_ptr(),
+                               lse.data_ptr(), sp)
+        assert st == 0, st
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        merge()
+    torch.cuda.synchronize(dev)
+    evs = []
+    with ClockSampler(0) as clk:
+        for _ in range(args.steps):
+            flush.zero_()
+            flush.view(torch.int32).sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            merge()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize(dev)
+    ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    nbytes = G * n * (R * 2 + 4) + n * (R * 2 + 4)
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    hbm, _, src = _peaks()
+    return {
+        "metric": "cross-shard LSE merge GB/s", "value": round(achieved, 1), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 parts, lse ~ 4 N(0,1))",
+        "config": {"workload": f"lse_merge G={G} rows={rows} H={H} R={R}",
+                   "l2": "flushed between steps (256 MiB write, then read back)"},
+        "roofline": {"bound": "hbm", "kernel": "lse_merge_kernel", "achieved": round(achieved, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": None, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs, burst)"},
+        "gpu_launches": args.steps, "clocks": clk.summary(),
+    }
+
+
 # ---------------------------------------------------------------- oracle timing
 def oracle_sample(workload: str, n_rows: int):
     """Time the oracle (as it stands) on the first n_rows rows of the workload:
@@ -432,12 +494,21 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4,
                     help="rows per step in the --impl reference sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["decode", "lse_merge"], default="decode",
+                    help="lse_merge: time the cross-shard merge alone (one GPU)")
+    ap.add_argument("--parts", type=int, default=8, help="--op lse_merge: shards G")
+    ap.add_argument("--merge-rows", type=int, default=64, help="--op lse_merge: rows")
+    ap.add_argument("--merge-heads", type=int, default=128, help="--op lse_merge: heads")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.op == "lse_merge":
+        if rank == 0 and args.impl == "ours":
+            print(json.dumps(run_lse_merge(args)), flush=True)
+        return
     if args.impl == "reference":
         line = run_reference(args, rank, world)
         if line is not None:

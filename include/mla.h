@@ -276,6 +276,47 @@ mla_status mla_decode_noalloc(const void* q, int64_t q_row_stride,
                               void* o, float* lse, int* err_count,
                               void* stream);
 
+/*
+ * mla_lse_merge - cross-shard LSE merge (decode context parallelism).
+ *
+ * With decode context parallelism each rank holds a disjoint shard of every
+ * sequence's KV tokens, decodes the same query vectors over its shard, and
+ * the per-shard (o, lse) pairs are combined through their log-sum-exp
+ * ([note] Design motivation: decode returns lse for the cross-shard merge,
+ * cp_lse_ag_out_rs; [api] decode with DCP all-gathers the q heads).  The
+ * arithmetic is the split merge's ([diff] triton_decode_attention.py,
+ * _fwd_kernel_stage2): for each (row, head) record, M = max over the parts
+ * of lse_g, o = sum e^{lse_g - M} o_g / sum e^{lse_g - M},
+ * lse = M + ln sum e^{lse_g - M}.  Parts with lse_g = -inf hold no tokens
+ * and are skipped; a record whose parts are all empty gets o = 0 and
+ * lse = -inf.  This call is the combine step alone, after the (o, lse) of
+ * every shard has been gathered onto this GPU; the exchange between ranks is
+ * the caller's.
+ *
+ * o_parts    device, bf16 [num_parts][num_rows][num_heads][kv_lora_rank]:
+ *            part g starts at element g * o_part_stride (a multiple of 8,
+ *            >= num_rows * num_heads * kv_lora_rank); rows and heads dense.
+ *            16-byte aligned.  Read only.
+ * lse_parts  device, fp32 [num_parts][num_rows][num_heads], natural log:
+ *            part g starts at element g * lse_part_stride
+ *            (>= num_rows * num_heads).  Read only.
+ * num_parts  1 .. 1024.  num_rows >= 0, num_heads 1 .. 128.
+ * kv_lora_rank  512 or 256 (else MLA_ERR_UNSUPPORTED).
+ * o          device, bf16 [num_rows][num_heads][kv_lora_rank], 16-byte
+ *            aligned; lse  device, fp32 [num_rows][num_heads].  Written; they
+ *            must not overlap the inputs.
+ * stream     cudaStream_t (NULL: the legacy default stream).
+ *
+ * Errors: MLA_ERR_INVALID_ARG for null pointers, misalignment or bad sizes
+ * (nothing launched); MLA_ERR_CUDA if the launch fails.  num_rows == 0 is a
+ * no-op returning MLA_OK.  Asynchronous: results are ready when the stream
+ * reaches the kernel.
+ */
+mla_status mla_lse_merge(const void* o_parts, int64_t o_part_stride,
+                         const float* lse_parts, int64_t lse_part_stride,
+                         int num_parts, int num_rows, int num_heads,
+                         int kv_lora_rank, void* o, float* lse, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* mla_status_string(mla_status status);
 

@@ -5,6 +5,8 @@ Thin Python binding over the C ABI of ``libmla.so`` (``include/mla.h``):
 * ``mla_cache_write``, ``mla_decode``, ``mla_decode_ex``,
   ``mla_num_kv_splits``, ``mla_decode_workspace_bytes`` — the C entry points
   under the same names, taking raw device pointers (ints) and a stream handle.
+* ``mla_lse_merge`` and ``lse_merge(...)`` — the cross-shard LSE merge of
+  per-shard (o, lse) pairs (decode context parallelism).
 * ``cache_write(...)`` and ``decode(...)`` — torch-tensor conveniences that
   only marshal pointers, strides and the current CUDA stream; every step of
   the computation runs in the library's CUDA kernels.
@@ -19,7 +21,8 @@ from ._lib import (MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_PATH_AUTO, MLA_PATH_MMA_SYN
 
 __all__ = [
     "mla_cache_write", "mla_decode", "mla_decode_ex", "mla_num_kv_splits",
-    "mla_decode_workspace_bytes", "cache_write", "decode", "MlaError", "load",
+    "mla_decode_workspace_bytes", "mla_lse_merge", "cache_write", "decode", "lse_merge",
+    "MlaError", "load",
     "MLA_KV_BF16", "MLA_KV_FP8_E4M3", "MLA_PATH_AUTO", "MLA_PATH_MMA_SYNC",
     "MLA_PATH_TCGEN05",
 ]
@@ -36,6 +39,10 @@ def mla_decode(*args) -> int:
 
 def mla_decode_ex(*args) -> int:
     return load().mla_decode_ex(*args)
+
+
+def mla_lse_merge(*args) -> int:
+    return load().mla_lse_merge(*args)
 
 
 def mla_num_kv_splits(max_seq_len: int, sm_count: int) -> int:
@@ -141,4 +148,26 @@ def decode(q, kv_cache, block_table, seq_lens, sm_scale: float, num_kv_splits: i
         err_count.data_ptr() if err_count is not None else None, _stream_ptr(stream),
         int(path))
     _lib.check(st, "mla_decode")
+    return out, lse
+
+
+def lse_merge(o_parts, lse_parts, *, out=None, lse=None, stream=None):
+    """Cross-shard LSE merge; returns (o [rows, H, R] bf16, lse [rows, H] fp32).
+
+    ``o_parts`` bf16 [G, rows, H, R] and ``lse_parts`` fp32 [G, rows, H]: the
+    (o, lse) of G disjoint KV token shards of the same query vectors, each
+    part dense in (rows, H, R) / (rows, H); lse = -inf marks an empty part.
+    """
+    torch = _torch()
+    G, rows, H, R = o_parts.shape
+    assert lse_parts.shape == (G, rows, H)
+    assert o_parts.stride()[1:] == (H * R, R, 1) and lse_parts.stride()[1:] == (H, 1)
+    if out is None:
+        out = torch.empty(rows, H, R, dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty(rows, H, dtype=torch.float32, device=o_parts.device)
+    st = load().mla_lse_merge(
+        o_parts.data_ptr(), o_parts.stride(0), lse_parts.data_ptr(), lse_parts.stride(0), G,
+        rows, H, R, out.data_ptr(), lse.data_ptr(), _stream_ptr(stream))
+    _lib.check(st, "mla_lse_merge")
     return out, lse

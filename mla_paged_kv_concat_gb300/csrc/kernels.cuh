@@ -89,4 +89,10 @@ int tc_split_group(const DecodeParams& p, int sm_count);
 // every split slot either holding a partial or with lse = -inf.
 cudaError_t launch_merge(const DecodeParams& p, int R, cudaStream_t stream);
 
+// Cross-shard LSE merge of num_parts bf16 (o, lse) results over disjoint KV
+// token shards: records = rows * H, parts at the given element strides.
+cudaError_t launch_lse_merge(const void* o_parts, int64_t o_part_stride, const float* lse_parts,
+                             int64_t lse_part_stride, int num_parts, int64_t records, int R,
+                             void* o, float* lse, cudaStream_t stream);
+
 }  // namespace mla

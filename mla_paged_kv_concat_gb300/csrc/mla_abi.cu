@@ -376,6 +376,28 @@ mla_status mla_decode_merge(int num_rows, int num_heads, int kv_lora_rank,
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 
+mla_status mla_lse_merge(const void* o_parts, int64_t o_part_stride,
+                         const float* lse_parts, int64_t lse_part_stride,
+                         int num_parts, int num_rows, int num_heads,
+                         int kv_lora_rank, void* o, float* lse, void* stream) {
+  if (num_parts < 1 || num_parts > 1024 || num_rows < 0 || num_heads < 1 || num_heads > 128)
+    return MLA_ERR_INVALID_ARG;
+  if (kv_lora_rank != 512 && kv_lora_rank != 256) return MLA_ERR_UNSUPPORTED;
+  if (num_rows == 0) return MLA_OK;
+  const int64_t records = static_cast<int64_t>(num_rows) * num_heads;
+  if (!o_parts || !lse_parts || !o || !lse || !aligned16(o_parts) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse_parts) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return MLA_ERR_INVALID_ARG;
+  if (o_part_stride % 8 != 0 || o_part_stride < records * kv_lora_rank ||
+      lse_part_stride < records)
+    return MLA_ERR_INVALID_ARG;
+  cudaError_t e = mla::launch_lse_merge(o_parts, o_part_stride, lse_parts, lse_part_stride,
+                                        num_parts, records, kv_lora_rank, o, lse,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e);
+}
+
 mla_status mla_decode_ex(const void* q, int64_t q_row_stride,
                          int64_t q_head_stride, int num_rows, int num_heads,
                          const void* kv_cache, mla_kv_dtype kv_dtype,

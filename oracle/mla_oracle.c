@@ -313,9 +313,9 @@ void oracle_decode(const uint16_t *q, int64_t q_row_stride,
  * split count from max_seq_len / 512, capped at sm_count * 2; [note] Data
  * flow: VLLM_BATCH_INVARIANT forces 1 split).  The body is not printed; the
  * plainest reading is min(ceil(max_seq_len / 512), 2 * sm_count), at least 1. */
-/* Cross-shard merge ([note] Data flow: with decode context parallelism each
- * rank attends over its shard of the KV tokens and cp_lse_ag_out_rs combines
- * the (o, lse) pairs; [api] decode with DCP all-gathers q heads first).  The
+/* Cross-shard merge ([note] Design motivation: decode returns lse because
+ * decode context parallelism merges the per-shard (o, lse) pairs with
+ * cp_lse_ag_out_rs; [api] decode with DCP all-gathers q heads first).  The
  * same LSE algebra as the split merge above: for each of n (row, head)
  * records, M = max over the G parts of lse_g (parts with lse = -inf hold no
  * tokens and are skipped), o = sum e^{lse_g - M} o_g / sum e^{lse_g - M},

@@ -98,3 +98,25 @@ def test_cache_write_rejects_bad_arguments(lib, over, code):
 def test_zero_work_is_ok_without_touching_memory(lib):
     assert lib.mla_cache_write(*_write_args(T=0, kv_c=None, slots=None)) == 0
     assert lib.mla_decode_ex(*_decode_args(rows=0)) == 0
+
+
+def _lse_merge_args(**over):
+    a = dict(o_parts=FAKE, ops=2 * 16 * 512, lse_parts=FAKE, lps=2 * 16, G=3, rows=2, H=16,
+             R=512, o=FAKE, lse=FAKE, stream=None)
+    a.update(over)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(o_parts=None), 1), (dict(lse_parts=None), 1), (dict(o=None), 1), (dict(lse=None), 1),
+    (dict(G=0), 1), (dict(G=1025), 1), (dict(H=0), 1), (dict(H=129), 1), (dict(rows=-1), 1),
+    (dict(R=384), 2), (dict(ops=2 * 16 * 512 - 8), 1), (dict(ops=2 * 16 * 512 + 4), 1),
+    (dict(lps=31), 1), (dict(o_parts=FAKE + 8), 1), (dict(o=FAKE + 8), 1),
+    (dict(lse=FAKE + 2), 1),
+])
+def test_lse_merge_rejects_bad_arguments(lib, over, code):
+    assert lib.mla_lse_merge(*_lse_merge_args(**over)) == code
+
+
+def test_lse_merge_zero_rows_is_a_noop(lib):
+    assert lib.mla_lse_merge(*_lse_merge_args(rows=0, o_parts=None, o=None)) == 0

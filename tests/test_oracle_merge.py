@@ -3,7 +3,7 @@
 What it restates: with decode context parallelism every rank attends over its
 shard of the KV tokens and the (o, lse) pairs are combined by their
 log-sum-exp ("Triton and MLA: portable attention and multi-head latent
-attention", Data flow: cp_lse_ag_out_rs; "vllm.v1.attention.backends.mla.
+attention", Design motivation: cp_lse_ag_out_rs; "vllm.v1.attention.backends.mla.
 triton_mla", decode with DCP).  Pinned against the direct definition: the
 decode of disjoint token shards, merged, equals the decode of the whole
 sequence; and against the closed forms of the special cases.
