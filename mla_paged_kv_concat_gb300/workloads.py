@@ -18,6 +18,11 @@ benchmark and the tests use:
 * ``long_multirow`` 8 sequences x 4 query rows, H=128, 512+64,
                   L ~ U{65536..131072}, 20000-block pool.
 
+``norm_rope_inputs`` adds, for a workload's written tokens, what the step
+upstream of the cache write consumes: the RMSNorm weight, eps, each token's
+position and an fp32 cos | sin table of standard rotary frequencies, plus a
+q_pe block to rotate.
+
 Memory that the method must never read (blocks outside any sequence, rows past
 a sequence's length inside its last block, block-table padding) is filled with
 NaN (bf16 0x7FC0, fp8 0x7F), so an unmasked read shows up as NaN.
@@ -201,6 +206,60 @@ def make_workload(name: str, *, seed: int, seq_lens, num_heads: int, rows_per_se
                     kv_scale=float(np.float32(kv_scale)), sm_scale=float(np.float32(sm_scale)),
                     seq_lens=sl, block_table=bt, kv_cache=cache, q=q, kv_c=kv_c, k_pe=k_pe,
                     slot_mapping=slots, meta={"seed": seed, "pool": pool, "write": write})
+
+
+@dataclass
+class NormRopeInputs:
+    """Inputs of the RMSNorm + rotary + cache-write step for a workload's T
+    written tokens: ``gamma`` bf16 [R] (torch CPU); ``eps`` (an fp32 value);
+    ``positions`` int64 [T]; ``table`` fp32 [max_position, P] with cos of
+    pair i in column i and sin in column P/2 + i; ``q_pe`` bf16 [T, H, P]
+    (torch CPU)."""
+    gamma: torch.Tensor
+    eps: float
+    positions: np.ndarray
+    table: np.ndarray
+    q_pe: torch.Tensor
+
+
+def norm_rope_inputs(w: Workload, *, seed: int, max_position: int | None = None,
+                     num_bad_positions: int = 0, table_scale: float = 1.0,
+                     rope_base: float = 10000.0, q_heads: int | None = None) -> NormRopeInputs:
+    """Seeded inputs for the step upstream of the cache write.
+
+    Positions: a sequence's newest token sits at L - 1 (write "newest"),
+    every token of a sequence at 0..L-1 (write "all"), otherwise uniform
+    over the table.  ``num_bad_positions`` of them are then moved outside
+    [0, max_position).  The table holds angles pos * rope_base^(-2i/P)
+    (plain rotary frequencies; any fp32 table is a valid input) times
+    ``table_scale``.
+    """
+    R, P = w.kv_lora_rank, w.rope_dim
+    T = w.slot_mapping.size
+    rng = _rng(seed, 5)
+    if max_position is None:
+        max_position = max(w.max_seq_len, 1) + 64
+    mode = w.meta.get("write")
+    if mode == "newest":
+        pos = np.array([int(L) - 1 for L in w.seq_lens if L > 0], np.int64)
+    elif mode == "all":
+        pos = np.concatenate([np.arange(int(L), dtype=np.int64) for L in w.seq_lens]) \
+            if w.num_seqs else np.zeros(0, np.int64)
+    else:
+        pos = rng.integers(0, max_position, size=T).astype(np.int64)
+    assert pos.size == T and (T == 0 or pos.max() < max_position)
+    if num_bad_positions:
+        idx = rng.choice(T, size=num_bad_positions, replace=False)
+        pos[idx] = np.where(np.arange(num_bad_positions) % 2 == 0, -1 - idx, max_position + idx)
+    inv = rope_base ** (-2.0 * np.arange(P // 2, dtype=np.float64) / P)
+    ang = np.arange(max_position, dtype=np.float64)[:, None] * inv[None, :]
+    table = (np.concatenate([np.cos(ang), np.sin(ang)], axis=1) * table_scale).astype(np.float32)
+    gamma = bf16_bits_from_f32((1.0 + 0.25 * rng.standard_normal(R)).astype(np.float32))
+    H = q_heads if q_heads is not None else w.num_heads
+    q_pe = randn_bf16(rng, (T, H, P))
+    return NormRopeInputs(gamma=bits_to_torch_bf16(gamma), eps=float(np.float32(1e-6)),
+                          positions=pos, table=np.ascontiguousarray(table),
+                          q_pe=bits_to_torch_bf16(q_pe))
 
 
 def make(name: str) -> Workload:

@@ -22,6 +22,21 @@ Parity status per function (what pins each one is in ``tests/test_oracle_*.py``)
                      logsumexp over the gathered K/V; L = 1 gives v exactly;
                      equal scores give the mean of v and lse = s + ln L;
                      brute-force fsum log-sum-exp; split route == direct route.
+* ``bf16_round``     pinned: every fp32 input against torch's RNE float ->
+                     bfloat16 cast (a single rounding there), and fp64 inputs
+                     where rounding through fp32 first would differ (listed
+                     ties, sticky bits below fp32, subnormals, overflow).
+* ``rms_norm``       pinned: torch CPU float64 ``rms_norm`` then one rounding;
+                     closed forms (constant rows give +-gamma exactly with
+                     eps = 0; power-of-two scaling leaves the output unchanged).
+* ``rope_interleaved`` pinned: numpy complex128 multiplication of the
+                     interleaved pairs by cos + i sin; cos = 1, sin = 0 is the
+                     identity and cos = 0, sin = 1 maps (a, b) to (-b, a)
+                     exactly; a rotation and its inverse restore the input.
+* ``norm_rope_cache_write`` composes the three with ``cache_write``; pinned
+                     by its special cases (padded slots rotate q_pe but write
+                     nothing; rows with a position outside the table are left
+                     untouched and counted).
 * ``num_kv_splits``  pinned: the rule's closed form at the cap, the floor and
                      the 512-token steps.
 """
@@ -69,6 +84,11 @@ def _load():
         lib.oracle_e4m3_encode_n.argtypes = [P, P, i64]
         lib.oracle_e4m3_value_n.argtypes = [P, P, i64]
         lib.oracle_bf16_value_n.argtypes = [P, P, i64]
+        lib.oracle_bf16_round_n.argtypes = [P, P, i64]
+        lib.oracle_rms_norm.argtypes = [P, i64, i64, i32, P, ctypes.c_double, P]
+        lib.oracle_rms_norm.restype = None
+        lib.oracle_rope_interleaved.argtypes = [P, i64, i64, i64, i32, i32, P, P, i64]
+        lib.oracle_rope_interleaved.restype = i64
         lib.oracle_cache_write.argtypes = [P, i64, P, i64, P, i64, i32, i32, P,
                                            i64, i32, i64, i32, f32]
         lib.oracle_cache_write.restype = i64
@@ -122,6 +142,64 @@ def e4m3_encode(y) -> np.ndarray:
     out = np.empty(v.shape, np.uint8)
     _load().oracle_e4m3_encode_n(_ptr(v), _ptr(out), v.size)
     return out
+
+
+def bf16_round(x) -> np.ndarray:
+    """fp64 -> bf16 bits, one rounding to nearest even."""
+    v = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty(v.shape, np.uint16)
+    _load().oracle_bf16_round_n(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def rms_norm(x, gamma, eps: float) -> np.ndarray:
+    """RMSNorm of bf16 rows ``x`` [n, R] with bf16 weight ``gamma`` [R];
+    returns bf16 bits [n, R]."""
+    xb, gb = _bits16(x), np.ascontiguousarray(_bits16(gamma))
+    assert xb.ndim == 2 and xb.strides[1] == 2
+    n, R = xb.shape
+    assert gb.shape == (R,)
+    out = np.empty((n, R), np.uint16)
+    _load().oracle_rms_norm(_ptr(xb), xb.strides[0] // 2, n, R, _ptr(gb), float(eps), _ptr(out))
+    return out
+
+
+def rope_interleaved(x: np.ndarray, positions, table) -> int:
+    """Rotate bf16 bits ``x`` [n, H, P] (uint16, last dim contiguous) in place by
+    ``positions`` [n] with the fp32 table [max_position, P] (cos | sin).
+    Returns the number of rows skipped for an out-of-range position."""
+    assert x.dtype == np.uint16 and x.ndim == 3 and x.strides[2] == 2
+    n, H, P = x.shape
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+    tab = np.ascontiguousarray(np.asarray(table, dtype=np.float32))
+    assert pos.shape == (n,) and tab.ndim == 2 and tab.shape[1] == P
+    return int(_load().oracle_rope_interleaved(_ptr(x), x.strides[0] // 2, x.strides[1] // 2,
+                                               n, H, P, _ptr(pos), _ptr(tab), tab.shape[0]))
+
+
+def norm_rope_cache_write(kv_c, k_pe, gamma, eps: float, positions, table, slot_mapping,
+                          kv_cache: np.ndarray, *, block_size: int, kv_lora_rank: int,
+                          rope_dim: int, kv_is_fp8: bool, scale: float = 1.0, q_pe=None):
+    """RMSNorm of kv_c, rotary embedding of k_pe (and of ``q_pe`` [T, H, P]
+    uint16, in place, when given), then the cache write of the results.  A
+    token whose position is outside the table is skipped entirely (nothing
+    written, its q_pe left as it is).  Returns (skipped slots, skipped
+    positions)."""
+    kc = _bits16(kv_c)
+    T = kc.shape[0]
+    normed = rms_norm(kc, gamma, eps)
+    rot = np.ascontiguousarray(_bits16(k_pe)[:, None, :rope_dim]).copy()
+    bad_pos = rope_interleaved(rot, positions, table)
+    if q_pe is not None:
+        assert q_pe.shape[0] == T
+        rope_interleaved(q_pe, positions, table)
+    pos = np.asarray(positions, dtype=np.int64)
+    slots = np.asarray(slot_mapping, dtype=np.int64).copy()
+    slots[(pos < 0) | (pos >= np.asarray(table).shape[0])] = -1
+    bad_slots = cache_write(normed, rot[:, 0, :], slots, kv_cache, block_size=block_size,
+                            kv_lora_rank=kv_lora_rank, rope_dim=rope_dim, kv_is_fp8=kv_is_fp8,
+                            scale=scale)
+    return bad_slots, bad_pos
 
 
 def num_kv_splits(max_seq_len: int, sm_count: int, deterministic: bool = False) -> int:

@@ -139,6 +139,101 @@ int64_t oracle_cache_write(const uint16_t *kv_c, int64_t kv_c_row_stride,
 }
 
 /* ------------------------------------------------------------------ */
+/* Upstream of the cache write: kv_a_layernorm and the rotary embedding */
+/* ------------------------------------------------------------------ */
+
+/* fp64 value -> bf16 bits, one rounding: to nearest, ties to even.  bf16 is
+ * binary32 cut to 8 significant bits (same exponent range, subnormals down
+ * to 2^-133).  The quantum at |x| is 2^(E-7) for |x| in [2^E, 2^(E+1)),
+ * E >= -126, and 2^-133 below 2^-126; |x| / quantum is exact in fp64, is
+ * rounded to the nearest integer with ties to even, and multiplied back.  A
+ * result of 2^128 or more is infinity.  NaN -> 0x7FC0. */
+uint16_t oracle_bf16_round(double x) {
+  if (isnan(x)) return 0x7FC0;
+  uint16_t sign = signbit(x) ? 0x8000 : 0x0000;
+  double a = fabs(x);
+  if (a == 0.0) return sign;
+  if (isinf(a)) return sign | 0x7F80;
+  int k;
+  (void)frexp(a, &k); /* a = m 2^k, m in [0.5, 1): a in [2^(k-1), 2^k) */
+  int E = k - 1;
+  double quantum = ldexp(1.0, (E < -126 ? -126 : E) - 7);
+  double n = a / quantum;
+  double fl = floor(n);
+  double frac = n - fl;
+  double r = fl;
+  if (frac > 0.5 || (frac == 0.5 && fmod(fl, 2.0) != 0.0)) r = fl + 1.0;
+  double v = r * quantum;
+  if (v >= ldexp(1.0, 128)) return sign | 0x7F80;
+  float f = (float)v; /* exact: at most 8 significant bits, in range */
+  uint32_t w;
+  memcpy(&w, &f, sizeof w);
+  return sign | (uint16_t)(w >> 16);
+}
+
+/* RMSNorm of each latent row before it is cached ([diff]
+ * vllm/model_executor/models/deepseek_v2.py: kv_a_layernorm =
+ * RMSNorm(kv_lora_rank, eps=rms_norm_eps), applied to kv_c in forward).  The
+ * pages print no body; the plain reading of RMSNorm:
+ *   out[d] = x[d] / sqrt(mean_d x[d]^2 + eps) * gamma[d],
+ * evaluated in fp64 and rounded once to bf16.  x rows at x_row_stride; out
+ * dense [n_rows][R]. */
+void oracle_rms_norm(const uint16_t *x, int64_t x_row_stride, int64_t n_rows, int R,
+                     const uint16_t *gamma, double eps, uint16_t *out) {
+  for (int64_t t = 0; t < n_rows; ++t) {
+    const uint16_t *xr = x + t * x_row_stride;
+    double ss = 0.0;
+    for (int d = 0; d < R; ++d) {
+      double v = oracle_bf16_value(xr[d]);
+      ss += v * v;
+    }
+    double inv = 1.0 / sqrt(ss / R + eps);
+    for (int d = 0; d < R; ++d)
+      out[t * R + d] =
+          oracle_bf16_round(oracle_bf16_value(xr[d]) * inv * oracle_bf16_value(gamma[d]));
+  }
+}
+
+/* Rotary embedding, non-NeoX ("GPT-J") style, in place ([diff]
+ * deepseek_v2.py: rotary_emb = get_rope(qk_rope_head_dim, ...,
+ * rope_type 'deepseek_yarn', is_neox_style=False); applied to q_pe and k_pe
+ * by input position before concat_and_cache_mla, MLA common forward).  The
+ * pages print neither the rotation nor the table.  Readings: non-NeoX
+ * rotates the interleaved pairs (x[2i], x[2i+1]), i < P/2, by the angle of
+ * pair i:
+ *   x'[2i]   = x[2i] cos_i - x[2i+1] sin_i
+ *   x'[2i+1] = x[2i+1] cos_i + x[2i] sin_i,
+ * with cos_i = table[pos][i] and sin_i = table[pos][P/2 + i] (the DeepSeek
+ * YaRN frequencies and magnitude scale are whatever the fp32 table holds);
+ * fp64 arithmetic, one rounding to bf16.  x is [n_rows][n_heads][P] bf16 at
+ * the given strides; every head of row t uses positions[t].  A row whose
+ * position is outside [0, max_position) is left as it is.  Returns the
+ * number of such rows. */
+int64_t oracle_rope_interleaved(uint16_t *x, int64_t row_stride, int64_t head_stride,
+                                int64_t n_rows, int n_heads, int P, const int64_t *positions,
+                                const float *table, int64_t max_position) {
+  int64_t bad = 0;
+  for (int64_t t = 0; t < n_rows; ++t) {
+    int64_t pos = positions[t];
+    if (pos < 0 || pos >= max_position) {
+      ++bad;
+      continue;
+    }
+    const float *cs = table + pos * P;
+    for (int h = 0; h < n_heads; ++h) {
+      uint16_t *v = x + t * row_stride + h * head_stride;
+      for (int i = 0; i < P / 2; ++i) {
+        double a = oracle_bf16_value(v[2 * i]), b = oracle_bf16_value(v[2 * i + 1]);
+        double c = cs[i], s = cs[P / 2 + i];
+        v[2 * i] = oracle_bf16_round(a * c - b * s);
+        v[2 * i + 1] = oracle_bf16_round(b * c + a * s);
+      }
+    }
+  }
+  return bad;
+}
+
+/* ------------------------------------------------------------------ */
 /* Decode                                                              */
 /* ------------------------------------------------------------------ */
 
@@ -374,4 +469,7 @@ void oracle_e4m3_value_n(const uint8_t *codes, double *out, int64_t n) {
 }
 void oracle_bf16_value_n(const uint16_t *bits, double *out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_value(bits[i]);
+}
+void oracle_bf16_round_n(const double *x, uint16_t *out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_round(x[i]);
 }
