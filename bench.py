@@ -168,11 +168,31 @@ def run_ours(args, rank, world, local_rank):
     sp = int(stream.cuda_stream)
     maxb = bt.shape[1]
 
-    def write(kv_c_t, k_pe_t, slots_t):
-        st = lib.mla_cache_write(kv_c_t.data_ptr(), kv_c_t.stride(0), k_pe_t.data_ptr(),
-                                 k_pe_t.stride(0), slots_t.data_ptr(), T, R, P,
-                                 cache.data_ptr(), nb, bs, bstride, kvd,
-                                 kv_scale.data_ptr(), err.data_ptr(), sp)
+    if args.fused_write:
+        # the write fused with RMSNorm of kv_c and the rotary embedding of k_pe
+        # (and of q's rope columns when every written token is a query row)
+        nr = W.norm_rope_inputs(w, seed=11)
+        nr_gamma = nr.gamma.to(dev)
+        nr_pos = torch.from_numpy(nr.positions).to(dev)
+        nr_table = torch.from_numpy(nr.table).to(dev)
+        rot_q = T == rows
+
+    def write(kv_c_t, k_pe_t, slots_t, q_t=None):
+        if args.fused_write:
+            qp = q_t[:, :, R:] if (rot_q and q_t is not None) else None
+            st = lib.mla_norm_rope_cache_write(
+                kv_c_t.data_ptr(), kv_c_t.stride(0), k_pe_t.data_ptr(), k_pe_t.stride(0),
+                slots_t.data_ptr(), T, R, P, cache.data_ptr(), nb, bs, bstride, kvd,
+                kv_scale.data_ptr(), nr_gamma.data_ptr(), nr.eps, nr_pos.data_ptr(),
+                nr_table.data_ptr(), nr_table.shape[0],
+                qp.data_ptr() if qp is not None else None, qp.stride(0) if qp is not None else 0,
+                qp.stride(1) if qp is not None else 0, H if qp is not None else 0,
+                err.data_ptr(), sp)
+        else:
+            st = lib.mla_cache_write(kv_c_t.data_ptr(), kv_c_t.stride(0), k_pe_t.data_ptr(),
+                                     k_pe_t.stride(0), slots_t.data_ptr(), T, R, P,
+                                     cache.data_ptr(), nb, bs, bstride, kvd,
+                                     kv_scale.data_ptr(), err.data_ptr(), sp)
         assert st == 0, st
 
     def stage1(q_t, bt_t, sl_t, o_t, lse_t):
@@ -198,7 +218,7 @@ def run_ours(args, rank, world, local_rank):
         # previous one drains (programmatic dependent launch).
         e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         e[0].record(stream)
-        write(kv_c, k_pe, slots)
+        write(kv_c, k_pe, slots, q)
         stage1(q, bt, sl, o, lse)
         merge(sl, o, lse)
         e[1].record(stream)
@@ -209,7 +229,7 @@ def run_ours(args, rank, world, local_rank):
         # times (the stage-1 time is the roofline's denominator).
         e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         e[0].record(stream)
-        write(kv_c, k_pe, slots)
+        write(kv_c, k_pe, slots, q)
         e[1].record(stream)
         stage1(q, bt, sl, o, lse)
         e[2].record(stream)
@@ -277,7 +297,7 @@ def run_ours(args, rank, world, local_rank):
         for dst, src in ((d_q, h_q), (d_bt, h_bt), (d_sl, h_sl), (d_kvc, h_kvc),
                          (d_kpe, h_kpe), (d_slots, h_slots)):
             dst.copy_(src, non_blocking=True)
-        write(d_kvc, d_kpe, d_slots)
+        write(d_kvc, d_kpe, d_slots, d_q)
         st = lib.mla_decode(d_q.data_ptr(), d_q.stride(0), d_q.stride(1), rows, H,
                             cache.data_ptr(), kvd, nb, bs, bstride, R, P, d_bt.data_ptr(),
                             d_bt.stride(0), maxb, d_sl.data_ptr(), seqs, w.sm_scale,
@@ -340,12 +360,14 @@ def run_ours(args, rank, world, local_rank):
             "kv_lora_rank": R, "rope_dim": P, "block_size": bs,
             "seq_lens": [int(w.seq_lens.min()), int(w.seq_lens.max())],
             "kv_tokens": int(w.seq_lens.sum()), "new_tokens": T, "num_kv_splits": S,
-            "parallelism": f"replicas x{world}", "l2": "flushed between steps (256 MiB write, then read back)",
+            "parallelism": f"replicas x{world}",
+            "write": "RMSNorm + rotary + cache write (fused)" if args.fused_write else "cache write", "l2": "flushed between steps (256 MiB write, then read back)",
         },
         "tflops": round(flops * n_units / (total_ms * 1e-3) / 1e12, 2),
         "rows_per_s": round(rows * n_units / (total_ms * 1e-3), 1),
         "step_roofline_frac": round(roof_t / (ms_step * 1e-3), 4),
-        "kernel_ms": {"cache_write": round(float(np.mean(t_write)), 5),
+        "kernel_ms": {("norm_rope_cache_write" if args.fused_write else "cache_write"):
+                      round(float(np.mean(t_write)), 5),
                       "decode_splitkv": round(s1_ms, 5),
                       "decode_merge": round(float(np.mean(t_merge)), 5)},
         "roofline": {"bound": "hbm",
@@ -494,6 +516,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4,
                     help="rows per step in the --impl reference sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused-write", action="store_true",
+                    help="the step's write also does RMSNorm of kv_c and the rotary embedding")
     ap.add_argument("--op", choices=["decode", "lse_merge"], default="decode",
                     help="lse_merge: time the cross-shard merge alone (one GPU)")
     ap.add_argument("--parts", type=int, default=8, help="--op lse_merge: shards G")

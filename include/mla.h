@@ -97,6 +97,59 @@ mla_status mla_cache_write(const void* kv_c, int64_t kv_c_row_stride,
                            int* err_count, void* stream);
 
 /*
+ * mla_norm_rope_cache_write - the cache write fused with the two steps the
+ * model runs just before it: RMSNorm of the latent and the rotary embedding
+ * of k_pe (and, optionally, of q_pe).
+ *
+ * Restates [diff] vllm/model_executor/models/deepseek_v2.py
+ * (kv_a_layernorm = RMSNorm(kv_lora_rank, eps=rms_norm_eps) on kv_c;
+ * rotary_emb = get_rope(qk_rope_head_dim, ..., rope_type 'deepseek_yarn',
+ * is_neox_style=False)) and the MLA common forward (q_pe, k_pe rotated by
+ * input position, then concat_and_cache_mla).  The pages print neither body;
+ * the readings taken: for each token t < num_tokens with p = positions[t],
+ *   kv_n[d]   = bf16( kv_c[t, d] / sqrt(mean_d kv_c[t, d]^2 + eps) * gamma[d] )
+ *   k_r[2i]   = bf16( k_pe[t, 2i] c_i - k_pe[t, 2i+1] s_i )
+ *   k_r[2i+1] = bf16( k_pe[t, 2i+1] c_i + k_pe[t, 2i] s_i ),  i < P/2,
+ * with c_i = table[p][i], s_i = table[p][P/2 + i] (any YaRN frequencies and
+ * magnitude scale live in the table), computed in fp32 and rounded once to
+ * bf16; then [kv_n | k_r] is stored at slot_mapping[t] exactly as
+ * mla_cache_write stores [kv_c | k_pe] (bf16 copy or E4M3(x / *scale)).
+ * With q_pe != NULL every head of q_pe[t] is rotated the same way, in place.
+ * kv_c and k_pe are not modified.
+ *
+ * Arguments as mla_cache_write, plus:
+ *   gamma          device bf16 [kv_lora_rank], the RMSNorm weight; 16-byte
+ *                  aligned.
+ *   eps            RMSNorm epsilon (>= 0).
+ *   positions      device int64 [num_tokens].
+ *   cos_sin_table  device fp32 [max_position][rope_dim]: cos | sin; 16-byte
+ *                  aligned.
+ *   q_pe           device bf16 [num_tokens][q_pe_heads][rope_dim] at row /
+ *                  head strides q_pe_row_stride / q_pe_head_stride (elements,
+ *                  multiples of 8; may be the rope columns of q), or NULL.
+ *                  16-byte aligned.
+ * Restrictions: rope_dim == 64; kv_lora_rank 512 or 256; kv_c, k_pe 16-byte
+ * aligned with row strides multiples of 8 (else MLA_ERR_INVALID_ARG).
+ * A token with a position outside [0, max_position) is skipped entirely
+ * (nothing written, q_pe untouched) and counted in *err_count, as is a slot
+ * >= num_blocks * block_size.  A padded token (slot -1) writes nothing but
+ * its q_pe is still rotated.
+ */
+mla_status mla_norm_rope_cache_write(const void* kv_c, int64_t kv_c_row_stride,
+                                     const void* k_pe, int64_t k_pe_row_stride,
+                                     const int64_t* slot_mapping, int num_tokens,
+                                     int kv_lora_rank, int rope_dim, void* kv_cache,
+                                     int num_blocks, int block_size,
+                                     int64_t block_stride, mla_kv_dtype kv_dtype,
+                                     const float* scale, const void* gamma,
+                                     float eps, const int64_t* positions,
+                                     const float* cos_sin_table,
+                                     int64_t max_position, void* q_pe,
+                                     int64_t q_pe_row_stride,
+                                     int64_t q_pe_head_stride, int q_pe_heads,
+                                     int* err_count, void* stream);
+
+/*
  * mla_num_kv_splits - the split-count rule.
  *
  * [note] Key files, _compute_num_kv_splits: the KV split count is taken from

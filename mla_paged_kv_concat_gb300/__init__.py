@@ -5,6 +5,8 @@ Thin Python binding over the C ABI of ``libmla.so`` (``include/mla.h``):
 * ``mla_cache_write``, ``mla_decode``, ``mla_decode_ex``,
   ``mla_num_kv_splits``, ``mla_decode_workspace_bytes`` — the C entry points
   under the same names, taking raw device pointers (ints) and a stream handle.
+* ``mla_norm_rope_cache_write`` and ``norm_rope_cache_write(...)`` — the cache
+  write fused with the RMSNorm of kv_c and the rotary embedding of k_pe / q_pe.
 * ``mla_lse_merge`` and ``lse_merge(...)`` — the cross-shard LSE merge of
   per-shard (o, lse) pairs (decode context parallelism).
 * ``cache_write(...)`` and ``decode(...)`` — torch-tensor conveniences that
@@ -21,7 +23,8 @@ from ._lib import (MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_PATH_AUTO, MLA_PATH_MMA_SYN
 
 __all__ = [
     "mla_cache_write", "mla_decode", "mla_decode_ex", "mla_num_kv_splits",
-    "mla_decode_workspace_bytes", "mla_lse_merge", "cache_write", "decode", "lse_merge",
+    "mla_decode_workspace_bytes", "mla_lse_merge", "mla_norm_rope_cache_write",
+    "cache_write", "norm_rope_cache_write", "decode", "lse_merge",
     "MlaError", "load",
     "MLA_KV_BF16", "MLA_KV_FP8_E4M3", "MLA_PATH_AUTO", "MLA_PATH_MMA_SYNC",
     "MLA_PATH_TCGEN05",
@@ -39,6 +42,10 @@ def mla_decode(*args) -> int:
 
 def mla_decode_ex(*args) -> int:
     return load().mla_decode_ex(*args)
+
+
+def mla_norm_rope_cache_write(*args) -> int:
+    return load().mla_norm_rope_cache_write(*args)
 
 
 def mla_lse_merge(*args) -> int:
@@ -108,6 +115,36 @@ def cache_write(kv_c, k_pe, kv_cache, slot_mapping, kv_cache_dtype: str | None =
         bstride, kvd, scale.data_ptr() if scale is not None else None,
         err_count.data_ptr() if err_count is not None else None, _stream_ptr(stream))
     _lib.check(st, "mla_cache_write")
+
+
+def norm_rope_cache_write(kv_c, k_pe, kv_cache, slot_mapping, gamma, eps: float, positions,
+                          cos_sin_table, q_pe=None, kv_cache_dtype: str | None = None,
+                          scale=None, err_count=None, stream=None) -> None:
+    """RMSNorm(kv_c) * gamma and the non-NeoX rotation of k_pe by position,
+    written into ``kv_cache`` at ``slot_mapping``; ``q_pe`` [T, H, 64] (bf16,
+    may be the rope columns of q) is rotated in place when given.
+
+    ``gamma`` bf16 [R]; ``positions`` int64 [T]; ``cos_sin_table`` fp32
+    [max_position, 64] (cos | sin); ``scale`` a device fp32 tensor (fp8
+    caches only).
+    """
+    kvd = _kv_dtype(kv_cache, kv_cache_dtype)
+    nb, bs, d, bstride = _cache_geom(kv_cache)
+    assert kv_c.stride(1) == 1 and k_pe.stride(1) == 1 and cos_sin_table.stride(1) == 1
+    R, P = kv_c.shape[1], k_pe.shape[1]
+    assert R + P == d and cos_sin_table.shape[1] == P
+    if q_pe is not None:
+        assert q_pe.stride(2) == 1 and q_pe.shape[0] >= slot_mapping.numel()
+    st = load().mla_norm_rope_cache_write(
+        kv_c.data_ptr(), kv_c.stride(0), k_pe.data_ptr(), k_pe.stride(0),
+        slot_mapping.data_ptr(), slot_mapping.numel(), R, P, kv_cache.data_ptr(), nb, bs,
+        bstride, kvd, scale.data_ptr() if scale is not None else None, gamma.data_ptr(),
+        float(eps), positions.data_ptr(), cos_sin_table.data_ptr(), cos_sin_table.shape[0],
+        q_pe.data_ptr() if q_pe is not None else None,
+        q_pe.stride(0) if q_pe is not None else 0, q_pe.stride(1) if q_pe is not None else 0,
+        q_pe.shape[1] if q_pe is not None else 0,
+        err_count.data_ptr() if err_count is not None else None, _stream_ptr(stream))
+    _lib.check(st, "mla_norm_rope_cache_write")
 
 
 def decode(q, kv_cache, block_table, seq_lens, sm_scale: float, num_kv_splits: int, *,

@@ -50,6 +50,9 @@ SIGNATURES = {
     "mla_decode_noalloc": (_I32, [_P, _I64, _I64, _I32, _I32, _P, _I32, _I32, _I32, _I64,
                                   _I32, _I32, _P, _I64, _I32, _P, _I32, _F32, _P, _I32, _P,
                                   _P, _P, _P]),
+    "mla_norm_rope_cache_write": (_I32, [_P, _I64, _P, _I64, _P, _I32, _I32, _I32, _P, _I32,
+                                         _I32, _I64, _I32, _P, _P, _F32, _P, _P, _I64, _P,
+                                         _I64, _I64, _I32, _P, _P]),
     "mla_lse_merge": (_I32, [_P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P]),
     "mla_status_string": (ctypes.c_char_p, [_I32]),
     "mla_last_cuda_error": (ctypes.c_char_p, []),

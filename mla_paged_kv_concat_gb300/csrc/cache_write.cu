@@ -7,6 +7,15 @@
 // a time with 16-byte vector loads and stores (a 576-element bf16 row is 72
 // such chunks), in a warp-stride loop over the tokens, and the E4M3 encoding
 // avoids the division except next to a rounding boundary (see quant2).
+//
+// The fused variant also does the two steps the model runs just before that
+// kernel ("frozenleaves/vllm compare v0.11.0...mla_cuda_graphs",
+// vllm/model_executor/models/deepseek_v2.py and the MLA common forward):
+// kv_a_layernorm (RMSNorm of kv_c, weight gamma) and rotary_emb (non-NeoX
+// rotation of k_pe, and optionally of q_pe in place, by the token's
+// position, with a caller-given fp32 cos | sin table).  The normalised and
+// rotated rows are rounded to bf16 and then stored exactly as the plain
+// write stores its inputs.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
@@ -32,6 +41,15 @@ struct CacheWriteArgs {
   int64_t block_stride;
   const float* scale;
   int* err_count;
+  // fused RMSNorm + rotary (NR variant only)
+  const uint16_t* gamma;  // bf16 [R]
+  float eps;
+  const int64_t* positions;  // [num_tokens]
+  const float* table;        // fp32 [max_position][P]: cos | sin
+  int64_t max_position;
+  uint16_t* q_pe;            // bf16 [num_tokens][q_heads][P] at the strides below, or null
+  int64_t q_pe_row_stride, q_pe_head_stride;
+  int q_heads;
 };
 
 constexpr int kWarpsPerCta = 8;
@@ -86,10 +104,38 @@ __device__ __forceinline__ uint8_t quant1(uint16_t bits, float s) {
       __nv_cvt_float_to_fp8(__fdiv_rn(x, s), __NV_SATFINITE, __NV_E4M3));
 }
 
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// RMSNorm of 8 latent elements: bf16(x * inv * gamma).
+__device__ __forceinline__ uint4 norm8(uint4 x, uint4 g, float inv) {
+  const uint32_t xv[4] = {x.x, x.y, x.z, x.w}, gv[4] = {g.x, g.y, g.z, g.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    o[k] = pack_bf16x2(bf_lo(xv[k]) * inv * bf_lo(gv[k]), bf_hi(xv[k]) * inv * bf_hi(gv[k]));
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Non-NeoX rotation of 4 interleaved pairs (8 bf16) by angles with the given
+// cos and sin: (a, b) -> (a c - b s, b c + a s), rounded to bf16.
+__device__ __forceinline__ uint4 rope8(uint4 x, float4 c, float4 s) {
+  const uint32_t xv[4] = {x.x, x.y, x.z, x.w};
+  const float cv[4] = {c.x, c.y, c.z, c.w}, sv[4] = {s.x, s.y, s.z, s.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float a = bf_lo(xv[k]), b = bf_hi(xv[k]);
+    o[k] = pack_bf16x2(a * cv[k] - b * sv[k], b * cv[k] + a * sv[k]);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // VEC: every source row and destination row starts on a 16-byte boundary, so
 // rows move as 16-byte chunks (8 elements); otherwise element by element.
-template <bool FP8, bool VEC>
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
+// NR: the fused RMSNorm + rotary variant (VEC layout, P = 64 only).
+template <bool FP8, bool VEC, bool NR = false>
+__global__ void __launch_bounds__(kWarpsPerCta * 32, NR ? 3 : 1)
     cache_write_kernel(const CacheWriteArgs a) {
   // The decode kernels that follow wait for this grid's completion before
   // they read anything; letting them launch now hides their launch latency.
@@ -105,11 +151,22 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
   // load latency.
   const int nwarps = gridDim.x * kWarpsPerCta;
   const int warp_id = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  // fused variant: this lane's RMSNorm weights (latent chunks lane and
+  // lane + 32), the same for every token
+  uint4 gm[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+  if constexpr (NR) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      if (lane + 32 * k < a.R / 8)
+        gm[k] = __ldg(reinterpret_cast<const uint4*>(a.gamma) + lane + 32 * k);
+  }
   for (int t0 = warp_id * kTokensPerWarp; t0 < a.num_tokens; t0 += nwarps * kTokensPerWarp) {
     if constexpr (VEC) {
       // lane l holds 16-byte chunks l, l + 32, l + 64 of each D-element row
       // (D <= 576: at most 3)
       const int nc = a.R / 8, np = a.P / 8;
+      // the position goes first: the table loads depend on it
+      const int64_t pos = NR ? __ldg(a.positions + t0) : 0;
       uint4 v[kTokensPerWarp][3];
       int64_t slot[kTokensPerWarp];
 #pragma unroll
@@ -128,6 +185,65 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
                                  : (c < nc + np ? __ldg(src_p + (c - nc)) : make_uint4(0, 0, 0, 0));
         }
         slot[j] = in ? __ldg(a.slot_mapping + t) : -1;
+      }
+      if constexpr (NR) {
+        static_assert(kTokensPerWarp == 1, "the fused variant moves one token per warp");
+        // every lane's 16-byte chunk of a P = 64 rotary row is pair group
+        // lane & 7 (the rope chunks start at a multiple of 32 chunks)
+        const int t = t0;
+        const bool pos_ok = pos >= 0 && pos < a.max_position;
+        const int sub = lane & 7;
+        const float4* cs = reinterpret_cast<const float4*>(a.table + (pos_ok ? pos : 0) * 64);
+        const float4 cv = __ldg(cs + sub), sv = __ldg(cs + 8 + sub);
+        if (!pos_ok) {
+          if (lane == 0 && a.err_count) atomicAdd(a.err_count, 1);
+          continue;  // the whole token is skipped
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const int c = lane + 32 * k;
+          if (c < nc) {
+            const uint32_t xv[4] = {v[0][k].x, v[0][k].y, v[0][k].z, v[0][k].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              ss += bf_lo(xv[e]) * bf_lo(xv[e]) + bf_hi(xv[e]) * bf_hi(xv[e]);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float inv = __frsqrt_rn(ss * (1.0f / static_cast<float>(a.R)) + a.eps);
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const int c = lane + 32 * k;
+          if (c < nc)
+            v[0][k] = norm8(v[0][k], gm[k < 2 ? k : 0], inv);
+          else if (c < nc + np)
+            v[0][k] = rope8(v[0][k], cv, sv);
+        }
+        if (a.q_pe != nullptr) {
+          // q_pe of this token: q_heads x 8 chunks, chunk lane + 32 i is
+          // pair group lane & 7 of head (lane + 32 i) / 8
+          const int nq = a.q_heads * 8;
+          uint16_t* qrow = a.q_pe + static_cast<int64_t>(t) * a.q_pe_row_stride;
+          for (int c0 = 0; c0 < nq; c0 += 128) {
+            uint4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int c = c0 + 32 * u + lane;
+              if (c < nq)
+                x[u] = *reinterpret_cast<const uint4*>(qrow + (c >> 3) * a.q_pe_head_stride +
+                                                       (c & 7) * 8);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int c = c0 + 32 * u + lane;
+              if (c < nq)
+                *reinterpret_cast<uint4*>(qrow + (c >> 3) * a.q_pe_head_stride + (c & 7) * 8) =
+                    rope8(x[u], cv, sv);
+            }
+          }
+        }
       }
 #pragma unroll
       for (int j = 0; j < kTokensPerWarp; ++j) {
@@ -202,6 +318,14 @@ cudaError_t launch_cache_write(const void* kv_c, int64_t kv_c_stride,
   a.block_stride = block_stride;
   a.scale = scale;
   a.err_count = err_count;
+  a.gamma = nullptr;
+  a.eps = 0.f;
+  a.positions = nullptr;
+  a.table = nullptr;
+  a.max_position = 0;
+  a.q_pe = nullptr;
+  a.q_pe_row_stride = a.q_pe_head_stride = 0;
+  a.q_heads = 0;
   const size_t elt = fp8 ? 1 : 2;
   auto al16 = [](uintptr_t x) { return (x & 15u) == 0; };
   const bool vec = al16(reinterpret_cast<uintptr_t>(kv_c)) &&
@@ -230,6 +354,53 @@ cudaError_t launch_cache_write(const void* kv_c, int64_t kv_c_stride,
     else
       cache_write_kernel<false, false><<<grid, block, 0, stream>>>(a);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_rope_cache_write(const void* kv_c, int64_t kv_c_stride, const void* k_pe,
+                                         int64_t k_pe_stride, const int64_t* slot_mapping,
+                                         int num_tokens, int R, void* cache, int num_blocks,
+                                         int block_size, int64_t block_stride, bool fp8,
+                                         const float* scale, const void* gamma, float eps,
+                                         const int64_t* positions, const float* table,
+                                         int64_t max_position, void* q_pe,
+                                         int64_t q_pe_row_stride, int64_t q_pe_head_stride,
+                                         int q_heads, int* err_count, cudaStream_t stream) {
+  if (num_tokens == 0) return cudaSuccess;
+  CacheWriteArgs a;
+  a.kv_c = static_cast<const uint16_t*>(kv_c);
+  a.kv_c_stride = kv_c_stride;
+  a.k_pe = static_cast<const uint16_t*>(k_pe);
+  a.k_pe_stride = k_pe_stride;
+  a.slot_mapping = slot_mapping;
+  a.num_tokens = num_tokens;
+  a.R = R;
+  a.P = 64;
+  a.cache = cache;
+  a.num_slots = static_cast<int64_t>(num_blocks) * block_size;
+  a.block_size = block_size;
+  a.block_stride = block_stride;
+  a.scale = scale;
+  a.err_count = err_count;
+  a.gamma = static_cast<const uint16_t*>(gamma);
+  a.eps = eps;
+  a.positions = positions;
+  a.table = table;
+  a.max_position = max_position;
+  a.q_pe = static_cast<uint16_t*>(q_pe);
+  a.q_pe_row_stride = q_pe_row_stride;
+  a.q_pe_head_stride = q_pe_head_stride;
+  a.q_heads = q_heads;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t need = (static_cast<int64_t>(num_tokens) + kWarpsPerCta - 1) / kWarpsPerCta;
+  const dim3 grid(static_cast<unsigned>(need < 8 * sms ? need : 8 * sms));
+  const dim3 block(kWarpsPerCta * 32);
+  if (fp8)
+    cache_write_kernel<true, true, true><<<grid, block, 0, stream>>>(a);
+  else
+    cache_write_kernel<false, true, true><<<grid, block, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -60,6 +60,19 @@ cudaError_t launch_cache_write(const void* kv_c, int64_t kv_c_stride,
                                const float* scale, int* err_count,
                                cudaStream_t stream);
 
+// The cache write fused with RMSNorm of kv_c (weight gamma) and the non-NeoX
+// rotation of k_pe (and of q_pe in place when q_pe is non-null) by position,
+// table fp32 [max_position][64] = cos | sin.  Rows 16-byte aligned, P = 64.
+cudaError_t launch_norm_rope_cache_write(const void* kv_c, int64_t kv_c_stride, const void* k_pe,
+                                         int64_t k_pe_stride, const int64_t* slot_mapping,
+                                         int num_tokens, int R, void* cache, int num_blocks,
+                                         int block_size, int64_t block_stride, bool fp8,
+                                         const float* scale, const void* gamma, float eps,
+                                         const int64_t* positions, const float* table,
+                                         int64_t max_position, void* q_pe,
+                                         int64_t q_pe_row_stride, int64_t q_pe_head_stride,
+                                         int q_heads, int* err_count, cudaStream_t stream);
+
 // Stage 1 on warp-level MMA (mma.sync m16n8k16), any head count.  `tmap` is
 // a 3-D tiled tensor map over the cache {R+P, block_size, num_blocks} with a
 // {64, min(block_size, 64), 1} box: 128-byte swizzle for bf16, none for fp8.

@@ -189,6 +189,52 @@ mla_status mla_cache_write(const void* kv_c, int64_t kv_c_row_stride,
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 
+mla_status mla_norm_rope_cache_write(const void* kv_c, int64_t kv_c_row_stride,
+                                     const void* k_pe, int64_t k_pe_row_stride,
+                                     const int64_t* slot_mapping, int num_tokens,
+                                     int kv_lora_rank, int rope_dim, void* kv_cache,
+                                     int num_blocks, int block_size,
+                                     int64_t block_stride, mla_kv_dtype kv_dtype,
+                                     const float* scale, const void* gamma,
+                                     float eps, const int64_t* positions,
+                                     const float* cos_sin_table,
+                                     int64_t max_position, void* q_pe,
+                                     int64_t q_pe_row_stride,
+                                     int64_t q_pe_head_stride, int q_pe_heads,
+                                     int* err_count, void* stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || block_size > 1024 ||
+      max_position <= 0 || !(eps >= 0.f))
+    return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (rope_dim != 64 || (kv_lora_rank != 512 && kv_lora_rank != 256))
+    return MLA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return MLA_OK;
+  if (!kv_c || !k_pe || !slot_mapping || !kv_cache || !gamma || !positions || !cos_sin_table)
+    return MLA_ERR_INVALID_ARG;
+  const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  if (fp8 && !scale) return MLA_ERR_INVALID_ARG;
+  if (kv_c_row_stride < kv_lora_rank || k_pe_row_stride < rope_dim ||
+      kv_c_row_stride % 8 != 0 || k_pe_row_stride % 8 != 0 || !aligned16(kv_c) ||
+      !aligned16(k_pe) || !aligned16(gamma) || !aligned16(cos_sin_table))
+    return MLA_ERR_INVALID_ARG;
+  const int D = kv_lora_rank + rope_dim;
+  const size_t elt = fp8 ? 1 : 2;
+  if (block_stride < static_cast<int64_t>(block_size) * D ||
+      (block_stride * elt) % 16 != 0 || !aligned16(kv_cache))
+    return MLA_ERR_INVALID_ARG;
+  if (q_pe != nullptr &&
+      (q_pe_heads < 1 || q_pe_heads > 1024 || !aligned16(q_pe) || q_pe_row_stride % 8 != 0 ||
+       q_pe_head_stride % 8 != 0 || q_pe_head_stride < rope_dim ||
+       q_pe_row_stride < static_cast<int64_t>(q_pe_heads) * rope_dim))
+    return MLA_ERR_INVALID_ARG;
+  cudaError_t e = mla::launch_norm_rope_cache_write(
+      kv_c, kv_c_row_stride, k_pe, k_pe_row_stride, slot_mapping, num_tokens, kv_lora_rank,
+      kv_cache, num_blocks, block_size, block_stride, fp8, scale, gamma, eps, positions,
+      cos_sin_table, max_position, q_pe, q_pe_row_stride, q_pe_head_stride,
+      q_pe != nullptr ? q_pe_heads : 0, err_count, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e);
+}
+
 namespace {
 
 // Validates a decode call and fills `p`; returns MLA_OK or the error.

@@ -120,3 +120,31 @@ def test_lse_merge_rejects_bad_arguments(lib, over, code):
 
 def test_lse_merge_zero_rows_is_a_noop(lib):
     assert lib.mla_lse_merge(*_lse_merge_args(rows=0, o_parts=None, o=None)) == 0
+
+
+def _nr_args(**over):
+    a = dict(kv_c=FAKE, kcs=512, k_pe=FAKE, kps=64, slots=FAKE, T=4, R=512, P=64,
+             cache=FAKE, nb=8, bs=64, bstride=64 * 576, kvd=0, scale=None, gamma=FAKE,
+             eps=1e-6, pos=FAKE, table=FAKE, maxpos=4096, q_pe=None, qrs=0, qhs=0, qh=0,
+             err=None, stream=None)
+    a.update(over)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(kv_c=None), 1), (dict(gamma=None), 1), (dict(pos=None), 1), (dict(table=None), 1),
+    (dict(slots=None), 1), (dict(cache=None), 1), (dict(T=-1), 1), (dict(maxpos=0), 1),
+    (dict(eps=-1.0), 1), (dict(eps=float("nan")), 1), (dict(P=32), 2), (dict(R=384), 2),
+    (dict(kvd=1, scale=None), 1), (dict(kcs=516), 1), (dict(kv_c=FAKE + 8), 1),
+    (dict(gamma=FAKE + 4), 1), (dict(table=FAKE + 4), 1), (dict(bstride=100), 1),
+    (dict(q_pe=FAKE, qrs=16 * 64, qhs=64, qh=0), 1),
+    (dict(q_pe=FAKE, qrs=16 * 64, qhs=60, qh=16), 1),
+    (dict(q_pe=FAKE, qrs=15 * 64, qhs=64, qh=16), 1),
+    (dict(q_pe=FAKE + 2, qrs=16 * 64, qhs=64, qh=16), 1),
+])
+def test_norm_rope_cache_write_rejects_bad_arguments(lib, over, code):
+    assert lib.mla_norm_rope_cache_write(*_nr_args(**over)) == code
+
+
+def test_norm_rope_cache_write_zero_tokens_is_a_noop(lib):
+    assert lib.mla_norm_rope_cache_write(*_nr_args(T=0, kv_c=None, slots=None)) == 0
