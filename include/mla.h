@@ -370,6 +370,103 @@ mla_status mla_lse_merge(const void* o_parts, int64_t o_part_stride,
                          int num_parts, int num_rows, int num_heads,
                          int kv_lora_rank, void* o, float* lse, void* stream);
 
+/*
+ * Decode plans: the validation, kernel choice and tensor-map encoding of a
+ * decode step done once, for steps that repeat with the same buffers.
+ *
+ * The pages run decode under CUDA graphs: the graph is captured once over
+ * fixed device buffers (slot_mapping, seq_lens, block_tables) and replayed
+ * after new values are copied into them ([diff] triton_mla.py,
+ * TritonMLAState: graph_capture, get_graph_input_buffers,
+ * prepare_graph_input_buffers).  A plan is that contract for this library:
+ * mla_plan_create checks every argument and prepares the launches;
+ * mla_plan_run only launches kernels (no allocation, no synchronisation, no
+ * host-side validation), so it may be captured into a CUDA graph and
+ * replayed.  Between runs the CONTENTS of every buffer may change (seq_lens
+ * up to max_blocks_per_seq * block_size, block ids, q, the new tokens), the
+ * pointers, shapes and num_kv_splits may not.  The stage-1 schedule is
+ * computed on the device from seq_lens at every run.
+ *
+ * The query may be given as one tensor holding all R+P dims (q_pe == NULL)
+ * or as the pair (q_nope, q_pe) without a concatenation: the pages' decode
+ * accepts q as a tensor or as a (q_nope, q_pe) tuple, which it concatenates
+ * ([note] Data flow, forward_mqa; this library reads both parts in
+ * place).
+ *
+ * A plan may include the cache write of the step's new tokens, plain
+ * (mla_cache_write) or fused with RMSNorm and the rotary embedding
+ * (gamma != NULL: mla_norm_rope_cache_write); with rotate_q != 0 the fused
+ * write also rotates the rope dims of the query in place (q_pe, or dims
+ * [R, R+P) of q), which needs num_tokens == num_rows (one new token per
+ * query row, in the same order).
+ *
+ * Every field has the meaning, layout and constraints of the argument of
+ * the same name in mla_decode_ex, mla_cache_write and
+ * mla_norm_rope_cache_write.  num_tokens == 0 means no write.  The plan
+ * copies the description; the caller keeps the buffers alive for as long as
+ * the plan runs.
+ */
+typedef struct {
+  /* query: dims [0, R) (all R+P when q_pe is NULL) */
+  const void* q;
+  int64_t q_row_stride, q_head_stride;
+  const void* q_pe; /* dims [R, R+P), or NULL */
+  int64_t q_pe_row_stride, q_pe_head_stride;
+  int num_rows, num_heads;
+  /* cache */
+  void* kv_cache;
+  mla_kv_dtype kv_dtype;
+  int num_blocks, block_size;
+  int64_t block_stride;
+  int kv_lora_rank, rope_dim;
+  const float* kv_scale;
+  /* batch */
+  const int32_t* block_table;
+  int64_t block_table_stride;
+  int max_blocks_per_seq;
+  const int32_t* seq_lens;
+  int num_seqs;
+  float sm_scale;
+  int num_kv_splits;
+  void* workspace;
+  size_t workspace_bytes;
+  void* o;
+  float* lse;
+  int* err_count;
+  mla_decode_path path;
+  /* cache write before stage 1 (num_tokens == 0: none) */
+  const void* kv_c;
+  int64_t kv_c_row_stride;
+  const void* k_pe;
+  int64_t k_pe_row_stride;
+  const int64_t* slot_mapping;
+  int num_tokens;
+  /* fused RMSNorm + rotary write when gamma != NULL */
+  const void* gamma;
+  float eps;
+  const int64_t* positions;
+  const float* cos_sin_table;
+  int64_t max_position;
+  int rotate_q;
+} mla_decode_desc;
+
+typedef struct mla_decode_plan mla_decode_plan; /* opaque, host memory */
+
+/* Validates *desc and prepares its launches.  On MLA_OK *plan is a new plan
+ * (release it with mla_plan_destroy); on error *plan is NULL and nothing was
+ * launched.  Call it with the plan's device current and outside any stream
+ * capture (it queries the device and encodes tensor maps). */
+mla_status mla_plan_create(const mla_decode_desc* desc, mla_decode_plan** plan);
+
+/* Launches the plan's step on `stream` (cudaStream_t; NULL: the legacy
+ * default stream): the write (if any), stage 1 and, with num_kv_splits > 1,
+ * the merge.  Asynchronous.  MLA_ERR_INVALID_ARG for a NULL plan,
+ * MLA_ERR_CUDA if a launch fails. */
+mla_status mla_plan_run(const mla_decode_plan* plan, void* stream);
+
+/* Frees a plan (NULL is ignored).  Launches already made are unaffected. */
+void mla_plan_destroy(mla_decode_plan* plan);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* mla_status_string(mla_status status);
 

@@ -7,6 +7,8 @@ Thin Python binding over the C ABI of ``libmla.so`` (``include/mla.h``):
   under the same names, taking raw device pointers (ints) and a stream handle.
 * ``mla_norm_rope_cache_write`` and ``norm_rope_cache_write(...)`` — the cache
   write fused with the RMSNorm of kv_c and the rotary embedding of k_pe / q_pe.
+* ``DecodePlan`` — ``mla_plan_create`` / ``mla_plan_run``: a validated step
+  over fixed tensors whose ``run()`` only launches kernels (CUDA-graph safe).
 * ``mla_lse_merge`` and ``lse_merge(...)`` — the cross-shard LSE merge of
   per-shard (o, lse) pairs (decode context parallelism).
 * ``cache_write(...)`` and ``decode(...)`` — torch-tensor conveniences that
@@ -24,7 +26,7 @@ from ._lib import (MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_PATH_AUTO, MLA_PATH_MMA_SYN
 __all__ = [
     "mla_cache_write", "mla_decode", "mla_decode_ex", "mla_num_kv_splits",
     "mla_decode_workspace_bytes", "mla_lse_merge", "mla_norm_rope_cache_write",
-    "cache_write", "norm_rope_cache_write", "decode", "lse_merge",
+    "cache_write", "norm_rope_cache_write", "decode", "lse_merge", "DecodePlan",
     "MlaError", "load",
     "MLA_KV_BF16", "MLA_KV_FP8_E4M3", "MLA_PATH_AUTO", "MLA_PATH_MMA_SYNC",
     "MLA_PATH_TCGEN05",
@@ -153,12 +155,25 @@ def decode(q, kv_cache, block_table, seq_lens, sm_scale: float, num_kv_splits: i
            stream=None, path: int = MLA_PATH_AUTO):
     """MLA decode; returns (o [rows, H, R] bf16, lse [rows, H] fp32).
 
-    ``q`` [rows, H, R+P] bf16; rows = len(seq_lens) * rows_per_seq.
-    ``kv_cache`` [NB, bs, R+P]; ``block_table`` int32 [seqs, max_blocks];
-    ``seq_lens`` int32 [seqs]; ``kv_scale`` device fp32 tensor for fp8 caches;
-    ``workspace`` a device buffer of at least ``mla_decode_workspace_bytes``
-    bytes (allocated here when omitted and needed).
+    ``q`` [rows, H, R+P] bf16, or the pair (q_nope [rows, H, R], q_pe
+    [rows, H, P]) read in place without a concatenation; rows =
+    len(seq_lens) * rows_per_seq.  ``kv_cache`` [NB, bs, R+P];
+    ``block_table`` int32 [seqs, max_blocks]; ``seq_lens`` int32 [seqs];
+    ``kv_scale`` device fp32 tensor for fp8 caches; ``workspace`` a device
+    buffer of at least ``mla_decode_workspace_bytes`` bytes (allocated here
+    when omitted and needed).
     """
+    if isinstance(q, (tuple, list)):
+        q_nope, q_pe = q
+        plan = DecodePlan(q_nope, kv_cache, block_table, seq_lens, sm_scale, num_kv_splits,
+                          q_pe=q_pe, kv_cache_dtype=kv_cache_dtype, kv_scale=kv_scale,
+                          workspace=workspace, out=out, lse=lse, err_count=err_count,
+                          path=path)
+        try:
+            plan.run(stream)
+        finally:
+            plan.close()
+        return plan.out, plan.lse
     torch = _torch()
     kvd = _kv_dtype(kv_cache, kv_cache_dtype)
     nb, bs, d, bstride = _cache_geom(kv_cache)
@@ -186,6 +201,99 @@ def decode(q, kv_cache, block_table, seq_lens, sm_scale: float, num_kv_splits: i
         int(path))
     _lib.check(st, "mla_decode")
     return out, lse
+
+
+class DecodePlan:
+    """A validated, prepared decode step over fixed tensors (``mla_plan_*``).
+
+    ``run()`` only launches kernels, so it can be captured into a CUDA graph
+    and replayed after new values are copied into the same tensors.  The
+    tensors are kept referenced for the plan's life.
+
+    ``q``: [rows, H, R+P] bf16, or dims [0, R) when ``q_pe`` [rows, H, P] is
+    given.  ``write``: optional dict(kv_c, k_pe, slot_mapping) of the step's
+    new tokens, written before stage 1; ``norm_rope``: optional dict(gamma,
+    eps, positions, cos_sin_table, rotate_q) that makes that write the fused
+    RMSNorm + rotary write (rotate_q also rotates the query's rope dims in
+    place).
+    """
+
+    def __init__(self, q, kv_cache, block_table, seq_lens, sm_scale: float, num_kv_splits: int,
+                 *, q_pe=None, kv_cache_dtype: str | None = None, kv_scale=None,
+                 workspace=None, out=None, lse=None, err_count=None,
+                 path: int = MLA_PATH_AUTO, write=None, norm_rope=None):
+        import ctypes
+        torch = _torch()
+        kvd = _kv_dtype(kv_cache, kv_cache_dtype)
+        nb, bs, d, bstride = _cache_geom(kv_cache)
+        rows, H, dq = q.shape
+        assert q.stride(2) == 1
+        if q_pe is not None:
+            R, P = dq, q_pe.shape[2]
+            assert q_pe.shape[:2] == (rows, H) and q_pe.stride(2) == 1
+        else:
+            R, P = d - 64, 64
+            assert dq == d
+        assert R + P == d
+        if out is None:
+            out = torch.empty(rows, H, R, dtype=torch.bfloat16, device=q.device)
+        if lse is None:
+            lse = torch.empty(rows, H, dtype=torch.float32, device=q.device)
+        need = mla_decode_workspace_bytes(rows, H, num_kv_splits, R)
+        if need and workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        self.out, self.lse = out, lse
+        self._keep = [q, q_pe, kv_cache, block_table, seq_lens, kv_scale, workspace, out, lse,
+                      err_count, write, norm_rope]
+        ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+        dd = _lib.DecodeDesc(
+            q=q.data_ptr(), q_row_stride=q.stride(0), q_head_stride=q.stride(1),
+            q_pe=ptr(q_pe), q_pe_row_stride=q_pe.stride(0) if q_pe is not None else 0,
+            q_pe_head_stride=q_pe.stride(1) if q_pe is not None else 0,
+            num_rows=rows, num_heads=H, kv_cache=kv_cache.data_ptr(), kv_dtype=kvd,
+            num_blocks=nb, block_size=bs, block_stride=bstride, kv_lora_rank=R, rope_dim=P,
+            kv_scale=ptr(kv_scale), block_table=block_table.data_ptr(),
+            block_table_stride=block_table.stride(0), max_blocks_per_seq=block_table.shape[1],
+            seq_lens=seq_lens.data_ptr(), num_seqs=seq_lens.numel(), sm_scale=float(sm_scale),
+            num_kv_splits=int(num_kv_splits), workspace=ptr(workspace),
+            workspace_bytes=workspace.numel() * workspace.element_size()
+            if workspace is not None else 0,
+            o=out.data_ptr(), lse=lse.data_ptr(), err_count=ptr(err_count), path=int(path))
+        if write is not None:
+            kv_c, k_pe, slots = write["kv_c"], write["k_pe"], write["slot_mapping"]
+            assert kv_c.stride(1) == 1 and k_pe.stride(1) == 1
+            dd.kv_c, dd.kv_c_row_stride = kv_c.data_ptr(), kv_c.stride(0)
+            dd.k_pe, dd.k_pe_row_stride = k_pe.data_ptr(), k_pe.stride(0)
+            dd.slot_mapping, dd.num_tokens = slots.data_ptr(), slots.numel()
+            if norm_rope is not None:
+                tab = norm_rope["cos_sin_table"]
+                assert tab.stride(1) == 1 and tab.shape[1] == P
+                dd.gamma = norm_rope["gamma"].data_ptr()
+                dd.eps = float(norm_rope["eps"])
+                dd.positions = norm_rope["positions"].data_ptr()
+                dd.cos_sin_table, dd.max_position = tab.data_ptr(), tab.shape[0]
+                dd.rotate_q = int(bool(norm_rope.get("rotate_q", False)))
+        handle = ctypes.c_void_p()
+        _lib.check(load().mla_plan_create(ctypes.byref(dd), ctypes.byref(handle)),
+                   "mla_plan_create")
+        self._handle = handle.value
+
+    def run(self, stream=None):
+        """Launch the step on ``stream`` (default: the current torch stream)."""
+        assert self._handle is not None, "plan closed"
+        _lib.check(load().mla_plan_run(self._handle, _stream_ptr(stream)), "mla_plan_run")
+        return self.out, self.lse
+
+    def close(self):
+        if getattr(self, "_handle", None) is not None:
+            load().mla_plan_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def lse_merge(o_parts, lse_parts, *, out=None, lse=None, stream=None):

@@ -26,6 +26,37 @@ MLA_PATH_AUTO = 0
 MLA_PATH_MMA_SYNC = 1
 MLA_PATH_TCGEN05 = 2
 
+
+
+class DecodeDesc(ctypes.Structure):
+    """mla_decode_desc (include/mla.h), field for field."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("q_row_stride", ctypes.c_int64),
+        ("q_head_stride", ctypes.c_int64),
+        ("q_pe", ctypes.c_void_p), ("q_pe_row_stride", ctypes.c_int64),
+        ("q_pe_head_stride", ctypes.c_int64),
+        ("num_rows", ctypes.c_int), ("num_heads", ctypes.c_int),
+        ("kv_cache", ctypes.c_void_p), ("kv_dtype", ctypes.c_int),
+        ("num_blocks", ctypes.c_int), ("block_size", ctypes.c_int),
+        ("block_stride", ctypes.c_int64),
+        ("kv_lora_rank", ctypes.c_int), ("rope_dim", ctypes.c_int),
+        ("kv_scale", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p), ("block_table_stride", ctypes.c_int64),
+        ("max_blocks_per_seq", ctypes.c_int),
+        ("seq_lens", ctypes.c_void_p), ("num_seqs", ctypes.c_int),
+        ("sm_scale", ctypes.c_float), ("num_kv_splits", ctypes.c_int),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("err_count", ctypes.c_void_p),
+        ("path", ctypes.c_int),
+        ("kv_c", ctypes.c_void_p), ("kv_c_row_stride", ctypes.c_int64),
+        ("k_pe", ctypes.c_void_p), ("k_pe_row_stride", ctypes.c_int64),
+        ("slot_mapping", ctypes.c_void_p), ("num_tokens", ctypes.c_int),
+        ("gamma", ctypes.c_void_p), ("eps", ctypes.c_float),
+        ("positions", ctypes.c_void_p), ("cos_sin_table", ctypes.c_void_p),
+        ("max_position", ctypes.c_int64), ("rotate_q", ctypes.c_int),
+    ]
+
+
 # Every exported symbol and its (restype, argtypes).
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -54,6 +85,9 @@ SIGNATURES = {
                                          _I32, _I64, _I32, _P, _P, _F32, _P, _P, _I64, _P,
                                          _I64, _I64, _I32, _P, _P]),
     "mla_lse_merge": (_I32, [_P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _P, _P, _P]),
+    "mla_plan_create": (_I32, [ctypes.POINTER(DecodeDesc), ctypes.POINTER(ctypes.c_void_p)]),
+    "mla_plan_run": (_I32, [_P, _P]),
+    "mla_plan_destroy": (None, [_P]),
     "mla_status_string": (ctypes.c_char_p, [_I32]),
     "mla_last_cuda_error": (ctypes.c_char_p, []),
 }

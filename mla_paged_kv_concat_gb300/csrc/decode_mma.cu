@@ -151,7 +151,7 @@ template <int R, bool FP8, int MT, bool PERSIST>
 __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
     decode_mma_kernel(const DecodeParams p,
                       const __grid_constant__ CUtensorMap tmap,
-                      const __grid_constant__ CUtensorMap qmap) {
+                      const __grid_constant__ QMaps qmap) {
   using C = MmaCfg<R, FP8, MT>;
   constexpr int D = C::D, NCH = C::NCH, NCW = C::NCW, STAGES = C::STAGES;
   constexpr int NT = R / 32;  // 8-column MMA tiles per warp in P.V
@@ -177,7 +177,10 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
   const int S = p.num_splits;
   if (threadIdx.x == NCW * 32) {
     tma_prefetch_desc(&tmap);
-    if (p.q_tma) tma_prefetch_desc(&qmap);
+    if (p.q_tma) {
+      tma_prefetch_desc(&qmap.nope);
+      tma_prefetch_desc(&qmap.pe);
+    }
   }
   // Launched overlapped with the previous kernel of the stream: nothing in
   // global memory is read before it has completed.
@@ -336,9 +339,12 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
           for (int i = 0; i < ntile; ++i) {
             const int v = v0 + 16 * i;
             const int row = sg.b * p.rows_per_seq + v / H, h0 = v % H;
-            for (int c = 0; c < NCH; ++c)
-              tma_load_3d(q_dst + c * C::QBOX + i * 2048, &qmap, &q_full[k & 1], c * 64, h0,
-                          row);
+            // dims [0, R) from q_nope, [R, R+P) from q_pe
+            for (int c = 0; c < NCH; ++c) {
+              const bool pe = c >= R / 64;
+              tma_load_3d(q_dst + c * C::QBOX + i * 2048, pe ? &qmap.pe : &qmap.nope,
+                          &q_full[k & 1], (pe ? c - R / 64 : c) * 64, h0, row);
+            }
           }
         }
       } else {
@@ -351,7 +357,9 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
           const uint16_t* src = p.q;
           if (v < nvec) {
             const int row = sg.b * p.rows_per_seq + v / H, h = v % H;
-            src = p.q + row * p.q_row_stride + h * p.q_head_stride + ch * 8;
+            src = ch < R / 8 ? p.q + row * p.q_row_stride + h * p.q_head_stride + ch * 8
+                             : p.q_pe + row * p.q_pe_row_stride + h * p.q_pe_head_stride +
+                                   (ch - R / 8) * 8;
           }
           cp_async16(s_q + (ch >> 3) * C::QBOX + sw128(qr, ch & 7), src, v < nvec ? 16u : 0u);
         }
@@ -656,7 +664,7 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
 }
 
 template <int R, bool FP8, int MT, bool PERSIST>
-cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmap, const CUtensorMap& qmap,
+cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmap, const QMaps& qmap,
                       int sm_count, cudaStream_t stream) {
   using C = MmaCfg<R, FP8, MT>;
   static bool attr_done = false;  // per instantiation; benign race
@@ -675,7 +683,7 @@ cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmap, const CUte
 }
 
 template <int R, bool FP8, int MT>
-cudaError_t launch_r2(const DecodeParams& p, const CUtensorMap& tmap, const CUtensorMap& qmap,
+cudaError_t launch_r2(const DecodeParams& p, const CUtensorMap& tmap, const QMaps& qmap,
                       int sm_count, cudaStream_t stream) {
   const int qblocks = (p.rows_per_seq * p.num_heads + 16 * MT - 1) / (16 * MT);
   const int64_t units = static_cast<int64_t>(qblocks) * p.num_seqs;
@@ -685,7 +693,7 @@ cudaError_t launch_r2(const DecodeParams& p, const CUtensorMap& tmap, const CUte
 }
 
 template <int R, bool FP8>
-cudaError_t launch_r(const DecodeParams& p, const CUtensorMap& tmap, const CUtensorMap& qmap,
+cudaError_t launch_r(const DecodeParams& p, const CUtensorMap& tmap, const QMaps& qmap,
                      int sm_count, cudaStream_t stream) {
   const int nvec = p.rows_per_seq * p.num_heads;
   if (nvec <= 16) return launch_r2<R, FP8, 1>(p, tmap, qmap, sm_count, stream);
@@ -695,7 +703,7 @@ cudaError_t launch_r(const DecodeParams& p, const CUtensorMap& tmap, const CUten
 }  // namespace
 
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap,
-                              const CUtensorMap& qmap, int R, bool fp8, int sm_count,
+                              const QMaps& qmap, int R, bool fp8, int sm_count,
                               cudaStream_t stream) {
   if (R == 512) return fp8 ? launch_r<512, true>(p, tmap, qmap, sm_count, stream)
                            : launch_r<512, false>(p, tmap, qmap, sm_count, stream);

@@ -591,13 +591,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       const int hd = valid_v ? v % H : 0;
       const int half = (nch + 1) / 2;
       const int q_lo = own ? h * half : 0, q_hi = own ? (h ? nch : half) : nch;
-      const uint4* src = reinterpret_cast<const uint4*>(
-          valid_v ? p.q + row * p.q_row_stride + hd * p.q_head_stride + c0 * 64 : p.q);
+      // dims [0, 512) come from q_nope, [512, 576) from q_pe
+      const uint16_t* qn = valid_v ? p.q + row * p.q_row_stride + hd * p.q_head_stride : p.q;
+      const uint16_t* qp =
+          valid_v ? p.q_pe + row * p.q_pe_row_stride + hd * p.q_pe_head_stride : p.q_pe;
       uint32_t r[2][32];
       auto load_chunk = [&](int c, uint32_t (&d)[32]) {
+        const int gc = c0 + c;  // 64-dim chunk of the 576-dim vector
+        const uint4* src =
+            reinterpret_cast<const uint4*>(gc < 8 ? qn + gc * 64 : qp + (gc - 8) * 64);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const uint4 x = valid_v ? __ldg(src + c * 8 + j) : make_uint4(0, 0, 0, 0);
+          const uint4 x = valid_v ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
           d[4 * j] = x.x;
           d[4 * j + 1] = x.y;
           d[4 * j + 2] = x.z;
@@ -623,10 +628,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     auto prefetch_q = [&](const TcSeg& sg) {
       const int v = sg.g * 128 + row_i;
       if (v >= nvec) return;
-      const uint16_t* src = p.q + (sg.b * p.rows_per_seq + v / H) * p.q_row_stride +
-                            (v % H) * p.q_head_stride + c0 * 64;
-      for (int c = 0; c < nch; ++c)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + c * 64));
+      const int row = sg.b * p.rows_per_seq + v / H, hd = v % H;
+      const uint16_t* qn = p.q + row * p.q_row_stride + hd * p.q_head_stride;
+      const uint16_t* qp = p.q_pe + row * p.q_pe_row_stride + hd * p.q_pe_head_stride;
+      for (int c = 0; c < nch; ++c) {
+        const int gc = c0 + c;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(gc < 8 ? qn + gc * 64 : qp + (gc - 8) * 64));
+      }
     };
 
     for_each_seg([&](const TcSeg& sg, int k, int n0, const TcSeg* next) -> bool {

@@ -14,8 +14,10 @@ constexpr int kMaxPersistUnits = 512;
 // Arguments of one decode call after host validation.  Pointers are device
 // memory.  rows = num_seqs * rows_per_seq.
 struct DecodeParams {
-  const uint16_t* q;  // bf16 [rows, H, R+P]
+  const uint16_t* q;     // bf16 [rows, H, >= R]: dims [0, R) of each query vector
   int64_t q_row_stride, q_head_stride;
+  const uint16_t* q_pe;  // bf16 [rows, H, >= P]: dims [R, R+P) (q + R for a concatenated q)
+  int64_t q_pe_row_stride, q_pe_head_stride;
   int num_rows, num_heads, rows_per_seq, num_seqs;
   const int32_t* block_table;
   int64_t bt_stride;
@@ -73,16 +75,23 @@ cudaError_t launch_norm_rope_cache_write(const void* kv_c, int64_t kv_c_stride, 
                                          int64_t q_pe_row_stride, int64_t q_pe_head_stride,
                                          int q_heads, int* err_count, cudaStream_t stream);
 
+// Tensor maps of the two parts of q for the warp-MMA kernel: q_nope
+// {R, H, rows} and q_pe {P, H, rows}, each with a {64, 16, 1} box and
+// 128-byte swizzle.
+struct QMaps {
+  CUtensorMap nope;
+  CUtensorMap pe;
+};
+
 // Stage 1 on warp-level MMA (mma.sync m16n8k16), any head count.  `tmap` is
 // a 3-D tiled tensor map over the cache {R+P, block_size, num_blocks} with a
 // {64, min(block_size, 64), 1} box: 128-byte swizzle for bf16, none for fp8.
-// With p.q_tma, `qmap` is a 3-D map over q {R+P, H, rows} with a {64, 16, 1}
-// box and 128-byte swizzle (heads a multiple of 16); otherwise it is unused
-// and Q is gathered with cp.async.  With num_kv_splits > 1 it runs
+// With p.q_tma, `qmap` holds the maps of q's two parts (heads a multiple of
+// 16); otherwise it is unused and Q is gathered with cp.async.  With num_kv_splits > 1 it runs
 // persistent, one CTA per SM (`sm_count`).  Launched overlapped with the
 // previous kernel of the stream.
 cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap,
-                              const CUtensorMap& qmap, int R, bool fp8, int sm_count,
+                              const QMaps& qmap, int R, bool fp8, int sm_count,
                               cudaStream_t stream);
 
 // Stage 1 on tcgen05/TMEM for bf16 caches with R = 512, 2-CTA clusters of 128

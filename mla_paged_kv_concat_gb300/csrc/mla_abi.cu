@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <new>
 
 #include "../../include/mla.h"
 #include "kernels.cuh"
@@ -158,13 +159,17 @@ size_t mla_decode_workspace_bytes(int num_rows, int num_heads,
          (static_cast<size_t>(kv_lora_rank) + 1) * sizeof(float);
 }
 
-mla_status mla_cache_write(const void* kv_c, int64_t kv_c_row_stride,
-                           const void* k_pe, int64_t k_pe_row_stride,
-                           const int64_t* slot_mapping, int num_tokens,
-                           int kv_lora_rank, int rope_dim, void* kv_cache,
-                           int num_blocks, int block_size, int64_t block_stride,
-                           mla_kv_dtype kv_dtype, const float* scale,
-                           int* err_count, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Validation (and, with do_launch, the launch) of the plain cache write.
+mla_status cache_write_impl(const void* kv_c, int64_t kv_c_row_stride, const void* k_pe,
+                            int64_t k_pe_row_stride, const int64_t* slot_mapping,
+                            int num_tokens, int kv_lora_rank, int rope_dim, void* kv_cache,
+                            int num_blocks, int block_size, int64_t block_stride,
+                            mla_kv_dtype kv_dtype, const float* scale, int* err_count,
+                            void* stream, bool do_launch) {
   if (num_tokens < 0 || kv_lora_rank <= 0 || rope_dim <= 0 ||
       num_blocks <= 0 || block_size <= 0 || block_size > 1024)
     return MLA_ERR_INVALID_ARG;
@@ -182,6 +187,7 @@ mla_status mla_cache_write(const void* kv_c, int64_t kv_c_row_stride,
   if (block_stride < static_cast<int64_t>(block_size) * D ||
       (block_stride * elt) % 16 != 0 || !aligned16(kv_cache))
     return MLA_ERR_INVALID_ARG;
+  if (!do_launch) return MLA_OK;
   cudaError_t e = mla::launch_cache_write(
       kv_c, kv_c_row_stride, k_pe, k_pe_row_stride, slot_mapping, num_tokens,
       kv_lora_rank, rope_dim, kv_cache, num_blocks, block_size, block_stride,
@@ -189,19 +195,16 @@ mla_status mla_cache_write(const void* kv_c, int64_t kv_c_row_stride,
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 
-mla_status mla_norm_rope_cache_write(const void* kv_c, int64_t kv_c_row_stride,
-                                     const void* k_pe, int64_t k_pe_row_stride,
-                                     const int64_t* slot_mapping, int num_tokens,
-                                     int kv_lora_rank, int rope_dim, void* kv_cache,
-                                     int num_blocks, int block_size,
-                                     int64_t block_stride, mla_kv_dtype kv_dtype,
-                                     const float* scale, const void* gamma,
-                                     float eps, const int64_t* positions,
-                                     const float* cos_sin_table,
-                                     int64_t max_position, void* q_pe,
-                                     int64_t q_pe_row_stride,
-                                     int64_t q_pe_head_stride, int q_pe_heads,
-                                     int* err_count, void* stream) {
+// Validation (and, with do_launch, the launch) of the fused write.
+mla_status nr_write_impl(const void* kv_c, int64_t kv_c_row_stride, const void* k_pe,
+                         int64_t k_pe_row_stride, const int64_t* slot_mapping, int num_tokens,
+                         int kv_lora_rank, int rope_dim, void* kv_cache, int num_blocks,
+                         int block_size, int64_t block_stride, mla_kv_dtype kv_dtype,
+                         const float* scale, const void* gamma, float eps,
+                         const int64_t* positions, const float* cos_sin_table,
+                         int64_t max_position, void* q_pe, int64_t q_pe_row_stride,
+                         int64_t q_pe_head_stride, int q_pe_heads, int* err_count, void* stream,
+                         bool do_launch) {
   if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || block_size > 1024 ||
       max_position <= 0 || !(eps >= 0.f))
     return MLA_ERR_INVALID_ARG;
@@ -227,6 +230,7 @@ mla_status mla_norm_rope_cache_write(const void* kv_c, int64_t kv_c_row_stride,
        q_pe_head_stride % 8 != 0 || q_pe_head_stride < rope_dim ||
        q_pe_row_stride < static_cast<int64_t>(q_pe_heads) * rope_dim))
     return MLA_ERR_INVALID_ARG;
+  if (!do_launch) return MLA_OK;
   cudaError_t e = mla::launch_norm_rope_cache_write(
       kv_c, kv_c_row_stride, k_pe, k_pe_row_stride, slot_mapping, num_tokens, kv_lora_rank,
       kv_cache, num_blocks, block_size, block_stride, fp8, scale, gamma, eps, positions,
@@ -235,11 +239,51 @@ mla_status mla_norm_rope_cache_write(const void* kv_c, int64_t kv_c_row_stride,
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 
+}  // namespace
+
+extern "C" {
+
+mla_status mla_cache_write(const void* kv_c, int64_t kv_c_row_stride,
+                           const void* k_pe, int64_t k_pe_row_stride,
+                           const int64_t* slot_mapping, int num_tokens,
+                           int kv_lora_rank, int rope_dim, void* kv_cache,
+                           int num_blocks, int block_size, int64_t block_stride,
+                           mla_kv_dtype kv_dtype, const float* scale,
+                           int* err_count, void* stream) {
+  return cache_write_impl(kv_c, kv_c_row_stride, k_pe, k_pe_row_stride, slot_mapping,
+                          num_tokens, kv_lora_rank, rope_dim, kv_cache, num_blocks, block_size,
+                          block_stride, kv_dtype, scale, err_count, stream, true);
+}
+
+mla_status mla_norm_rope_cache_write(const void* kv_c, int64_t kv_c_row_stride,
+                                     const void* k_pe, int64_t k_pe_row_stride,
+                                     const int64_t* slot_mapping, int num_tokens,
+                                     int kv_lora_rank, int rope_dim, void* kv_cache,
+                                     int num_blocks, int block_size,
+                                     int64_t block_stride, mla_kv_dtype kv_dtype,
+                                     const float* scale, const void* gamma,
+                                     float eps, const int64_t* positions,
+                                     const float* cos_sin_table,
+                                     int64_t max_position, void* q_pe,
+                                     int64_t q_pe_row_stride,
+                                     int64_t q_pe_head_stride, int q_pe_heads,
+                                     int* err_count, void* stream) {
+  return nr_write_impl(kv_c, kv_c_row_stride, k_pe, k_pe_row_stride, slot_mapping, num_tokens,
+                       kv_lora_rank, rope_dim, kv_cache, num_blocks, block_size, block_stride,
+                       kv_dtype, scale, gamma, eps, positions, cos_sin_table, max_position,
+                       q_pe, q_pe_row_stride, q_pe_head_stride, q_pe_heads, err_count, stream,
+                       true);
+}
+
+}  // extern "C"
+
 namespace {
 
 // Validates a decode call and fills `p`; returns MLA_OK or the error.
 mla_status prepare_decode(const void* q, int64_t q_row_stride,
-                          int64_t q_head_stride, int num_rows, int num_heads,
+                          int64_t q_head_stride, const void* q_pe,
+                          int64_t q_pe_row_stride, int64_t q_pe_head_stride,
+                          int num_rows, int num_heads,
                           const void* kv_cache, mla_kv_dtype kv_dtype,
                           int num_blocks, int block_size, int64_t block_stride,
                           int kv_lora_rank, int rope_dim,
@@ -272,9 +316,14 @@ mla_status prepare_decode(const void* q, int64_t q_row_stride,
   if (!q || !kv_cache || !block_table || !seq_lens || !o || !lse)
     return MLA_ERR_INVALID_ARG;
   if (fp8 && !kv_scale) return MLA_ERR_INVALID_ARG;
+  // q alone holds all R+P dims, or q holds [0, R) and q_pe [R, R+P)
   if (!aligned16(q) || q_row_stride % 8 != 0 || q_head_stride % 8 != 0 ||
-      q_head_stride < D ||
+      q_head_stride < (q_pe ? kv_lora_rank : D) ||
       q_row_stride < static_cast<int64_t>(num_heads) * q_head_stride)
+    return MLA_ERR_INVALID_ARG;
+  if (q_pe && (!aligned16(q_pe) || q_pe_row_stride % 8 != 0 || q_pe_head_stride % 8 != 0 ||
+               q_pe_head_stride < rope_dim ||
+               q_pe_row_stride < static_cast<int64_t>(num_heads) * q_pe_head_stride))
     return MLA_ERR_INVALID_ARG;
   if (block_stride < static_cast<int64_t>(block_size) * D ||
       (block_stride * elt) % 16 != 0 || !aligned16(kv_cache))
@@ -298,6 +347,15 @@ mla_status prepare_decode(const void* q, int64_t q_row_stride,
   p->q = static_cast<const uint16_t*>(q);
   p->q_row_stride = q_row_stride;
   p->q_head_stride = q_head_stride;
+  if (q_pe) {
+    p->q_pe = static_cast<const uint16_t*>(q_pe);
+    p->q_pe_row_stride = q_pe_row_stride;
+    p->q_pe_head_stride = q_pe_head_stride;
+  } else {
+    p->q_pe = p->q + kv_lora_rank;
+    p->q_pe_row_stride = q_row_stride;
+    p->q_pe_head_stride = q_head_stride;
+  }
   p->num_rows = num_rows;
   p->num_heads = num_heads;
   p->rows_per_seq = num_rows / num_seqs;
@@ -332,30 +390,63 @@ bool use_tc(const mla::DecodeParams& p, bool fp8, int R, mla_decode_path path) {
          static_cast<int64_t>(p.rows_per_seq) * p.num_heads >= 128;
 }
 
+// Everything stage 1 needs at launch time, computed once per call (or once
+// per plan).
+struct Stage1 {
+  mla::DecodeParams p;
+  CUtensorMap tmap;
+  mla::QMaps qmaps;
+  bool tc, fp8;
+  int R, split_group, sm_count;
+};
+
+mla_status build_stage1(const mla::DecodeParams& p_in, const void* kv_cache, bool fp8, int R,
+                        int block_size, int num_blocks, int64_t block_stride,
+                        mla_decode_path path, Stage1* s1) {
+  s1->p = p_in;
+  s1->fp8 = fp8;
+  s1->R = R;
+  s1->sm_count = device_sm_count();
+  s1->tc = use_tc(s1->p, fp8, R, path);
+  mla_status st = make_cache_tmap(&s1->tmap, kv_cache, fp8, R + 64, block_size, num_blocks,
+                                  block_stride, 64);
+  if (st != MLA_OK) return st;
+  memset(&s1->qmaps, 0, sizeof s1->qmaps);
+  s1->p.q_tma = 0;
+  if (!s1->tc) {
+    const mla::DecodeParams& p = s1->p;
+    s1->p.q_tma = make_q_tmap(&s1->qmaps.nope, p.q, R, p.num_heads, p.num_rows,
+                              p.q_head_stride, p.q_row_stride) &&
+                          make_q_tmap(&s1->qmaps.pe, p.q_pe, 64, p.num_heads, p.num_rows,
+                                      p.q_pe_head_stride, p.q_pe_row_stride)
+                      ? 1
+                      : 0;
+  }
+  s1->split_group = s1->tc ? mla::tc_split_group(s1->p, s1->sm_count) : 1;
+  return MLA_OK;
+}
+
+mla_status launch_stage1(const Stage1& s1, cudaStream_t s) {
+  cudaError_t e = s1.tc ? mla::launch_decode_tc(s1.p, s1.tmap, s1.split_group, s1.sm_count, s)
+                        : mla::launch_decode_mma(s1.p, s1.tmap, s1.qmaps, s1.R, s1.fp8,
+                                                 s1.sm_count, s);
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e);
+}
+
 mla_status run_stage1(const mla::DecodeParams& p_in, const void* kv_cache,
                       bool fp8, int R, int block_size, int num_blocks,
                       int64_t block_stride, mla_decode_path path,
                       cudaStream_t s) {
-  mla::DecodeParams p = p_in;
-  CUtensorMap tmap, qmap;
-  const bool tc = use_tc(p, fp8, R, path);
-  mla_status st = make_cache_tmap(&tmap, kv_cache, fp8, R + 64, block_size,
-                                  num_blocks, block_stride, 64);
+  Stage1 s1;
+  mla_status st =
+      build_stage1(p_in, kv_cache, fp8, R, block_size, num_blocks, block_stride, path, &s1);
   if (st != MLA_OK) return st;
-  memset(&qmap, 0, sizeof qmap);
-  if (!tc)
-    p.q_tma = make_q_tmap(&qmap, p.q, R + 64, p.num_heads, p.num_rows, p.q_head_stride,
-                          p.q_row_stride)
-                  ? 1
-                  : 0;
-  cudaError_t e =
-      tc ? mla::launch_decode_tc(p, tmap, mla::tc_split_group(p, device_sm_count()),
-                                  device_sm_count(), s)
-         : mla::launch_decode_mma(p, tmap, qmap, R, fp8, device_sm_count(), s);
-  return e == cudaSuccess ? MLA_OK : cuda_fail(e);
+  return launch_stage1(s1, s);
 }
 
 }  // namespace
+
+extern "C" {
 
 mla_status mla_decode_splitkv(const void* q, int64_t q_row_stride,
                               int64_t q_head_stride, int num_rows,
@@ -373,7 +464,7 @@ mla_status mla_decode_splitkv(const void* q, int64_t q_row_stride,
                               mla_decode_path path) {
   mla::DecodeParams p;
   mla_status st = prepare_decode(
-      q, q_row_stride, q_head_stride, num_rows, num_heads, kv_cache, kv_dtype,
+      q, q_row_stride, q_head_stride, nullptr, 0, 0, num_rows, num_heads, kv_cache, kv_dtype,
       num_blocks, block_size, block_stride, kv_lora_rank, rope_dim,
       block_table, block_table_stride, max_blocks_per_seq, seq_lens, num_seqs,
       sm_scale, kv_scale, num_kv_splits, workspace, workspace_bytes, o, lse,
@@ -458,7 +549,7 @@ mla_status mla_decode_ex(const void* q, int64_t q_row_stride,
                          mla_decode_path path) {
   mla::DecodeParams p;
   mla_status st = prepare_decode(
-      q, q_row_stride, q_head_stride, num_rows, num_heads, kv_cache, kv_dtype,
+      q, q_row_stride, q_head_stride, nullptr, 0, 0, num_rows, num_heads, kv_cache, kv_dtype,
       num_blocks, block_size, block_stride, kv_lora_rank, rope_dim,
       block_table, block_table_stride, max_blocks_per_seq, seq_lens, num_seqs,
       sm_scale, kv_scale, num_kv_splits, workspace, workspace_bytes, o, lse,
@@ -493,5 +584,100 @@ mla_status mla_decode(const void* q, int64_t q_row_stride,
                        kv_scale, num_kv_splits, workspace, workspace_bytes, o,
                        lse, err_count, stream, MLA_PATH_AUTO);
 }
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ plans
+
+struct mla_decode_plan {
+  mla_decode_desc d;
+  bool has_stage1;
+  Stage1 s1;
+};
+
+namespace {
+
+// The plan's write: plain or fused, validated only (do_launch false) or run.
+mla_status plan_write(const mla_decode_desc& d, void* stream, bool do_launch) {
+  if (d.num_tokens == 0) return MLA_OK;
+  if (!d.gamma)
+    return cache_write_impl(d.kv_c, d.kv_c_row_stride, d.k_pe, d.k_pe_row_stride,
+                            d.slot_mapping, d.num_tokens, d.kv_lora_rank, d.rope_dim,
+                            d.kv_cache, d.num_blocks, d.block_size, d.block_stride, d.kv_dtype,
+                            d.kv_scale, d.err_count, stream, do_launch);
+  void* qr = nullptr;
+  int64_t qr_rs = 0, qr_hs = 0;
+  if (d.rotate_q) {
+    if (d.q_pe) {
+      qr = const_cast<void*>(d.q_pe);
+      qr_rs = d.q_pe_row_stride;
+      qr_hs = d.q_pe_head_stride;
+    } else {
+      qr = static_cast<uint16_t*>(const_cast<void*>(d.q)) + d.kv_lora_rank;
+      qr_rs = d.q_row_stride;
+      qr_hs = d.q_head_stride;
+    }
+  }
+  return nr_write_impl(d.kv_c, d.kv_c_row_stride, d.k_pe, d.k_pe_row_stride, d.slot_mapping,
+                       d.num_tokens, d.kv_lora_rank, d.rope_dim, d.kv_cache, d.num_blocks,
+                       d.block_size, d.block_stride, d.kv_dtype, d.kv_scale, d.gamma, d.eps,
+                       d.positions, d.cos_sin_table, d.max_position, qr, qr_rs, qr_hs,
+                       d.num_heads, d.err_count, stream, do_launch);
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_plan_create(const mla_decode_desc* desc, mla_decode_plan** plan) {
+  if (!plan) return MLA_ERR_INVALID_ARG;
+  *plan = nullptr;
+  if (!desc) return MLA_ERR_INVALID_ARG;
+  const mla_decode_desc& d = *desc;
+  if (d.num_tokens < 0) return MLA_ERR_INVALID_ARG;
+  if (d.num_tokens > 0 && d.gamma && d.rotate_q &&
+      (d.num_tokens != d.num_rows || d.q == nullptr))
+    return MLA_ERR_INVALID_ARG;
+  mla_status st = plan_write(d, nullptr, false);
+  if (st != MLA_OK) return st;
+  mla::DecodeParams p;
+  st = prepare_decode(d.q, d.q_row_stride, d.q_head_stride, d.q_pe, d.q_pe_row_stride,
+                      d.q_pe_head_stride, d.num_rows, d.num_heads, d.kv_cache, d.kv_dtype,
+                      d.num_blocks, d.block_size, d.block_stride, d.kv_lora_rank, d.rope_dim,
+                      d.block_table, d.block_table_stride, d.max_blocks_per_seq, d.seq_lens,
+                      d.num_seqs, d.sm_scale, d.kv_scale, d.num_kv_splits, d.workspace,
+                      d.workspace_bytes, d.o, d.lse, d.err_count, d.path, &p);
+  if (st != MLA_OK) return st;
+  mla_decode_plan* pl = new (std::nothrow) mla_decode_plan;
+  if (!pl) return MLA_ERR_INVALID_ARG;
+  pl->d = d;
+  pl->has_stage1 = d.num_rows > 0;
+  if (pl->has_stage1) {
+    st = build_stage1(p, d.kv_cache, d.kv_dtype == MLA_KV_FP8_E4M3, d.kv_lora_rank,
+                      d.block_size, d.num_blocks, d.block_stride, d.path, &pl->s1);
+    if (st != MLA_OK) {
+      delete pl;
+      return st;
+    }
+  }
+  *plan = pl;
+  return MLA_OK;
+}
+
+mla_status mla_plan_run(const mla_decode_plan* plan, void* stream) {
+  if (!plan) return MLA_ERR_INVALID_ARG;
+  mla_status st = plan_write(plan->d, stream, true);
+  if (st != MLA_OK || !plan->has_stage1) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = launch_stage1(plan->s1, s);
+  if (st != MLA_OK) return st;
+  if (plan->d.num_kv_splits > 1) {
+    cudaError_t e = mla::launch_merge(plan->s1.p, plan->d.kv_lora_rank, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return MLA_OK;
+}
+
+void mla_plan_destroy(mla_decode_plan* plan) { delete plan; }
 
 }  // extern "C"

@@ -4,6 +4,7 @@ run without a GPU)."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -148,3 +149,51 @@ def test_norm_rope_cache_write_rejects_bad_arguments(lib, over, code):
 
 def test_norm_rope_cache_write_zero_tokens_is_a_noop(lib):
     assert lib.mla_norm_rope_cache_write(*_nr_args(T=0, kv_c=None, slots=None)) == 0
+
+
+def test_decode_desc_layout_matches_the_header():
+    """The ctypes mirror of mla_decode_desc has the C compiler's field offsets."""
+    fields = [f for f, _ in _lib.DecodeDesc._fields_]
+    src = ['#include <stdio.h>', '#include <stddef.h>', '#include "mla.h"', 'int main(void) {',
+           'printf("%zu\\n", sizeof(mla_decode_desc));']
+    src += [f'printf("%zu\\n", offsetof(mla_decode_desc, {f}));' for f in fields]
+    src += ['return 0; }']
+    out = os.path.join(ROOT, "_build", "desc_layout")
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    with open(out + ".c", "w") as f:
+        f.write("\n".join(src) + "\n")
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), out + ".c", "-o", out],
+                   check=True, capture_output=True)
+    got = [int(x) for x in subprocess.run([out], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(_lib.DecodeDesc)
+    assert got[1:] == [getattr(_lib.DecodeDesc, f).offset for f in fields]
+
+
+def test_plan_create_validates_before_anything_runs(lib):
+    plan = ctypes.c_void_p(123)
+    assert lib.mla_plan_create(None, ctypes.byref(plan)) == 1 and plan.value is None
+    d = _lib.DecodeDesc(q=FAKE, q_row_stride=16 * 576, q_head_stride=576, num_rows=2,
+                        num_heads=16, kv_cache=FAKE, num_blocks=8, block_size=64,
+                        block_stride=64 * 576, kv_lora_rank=512, rope_dim=64, block_table=FAKE,
+                        block_table_stride=4, max_blocks_per_seq=4, seq_lens=FAKE, num_seqs=2,
+                        sm_scale=0.07, num_kv_splits=1, o=FAKE, lse=FAKE)
+    bad = [dict(q=None), dict(num_heads=129), dict(kv_lora_rank=384), dict(q_head_stride=512),
+           dict(q_head_stride=512, q_pe=FAKE, q_pe_row_stride=16 * 64, q_pe_head_stride=60),
+           dict(q_pe=FAKE + 2, q_head_stride=512, q_pe_row_stride=16 * 64, q_pe_head_stride=64),
+           dict(num_tokens=2, kv_c=None, k_pe=FAKE, slot_mapping=FAKE, kv_c_row_stride=512,
+                k_pe_row_stride=64),
+           dict(num_tokens=3, kv_c=FAKE, k_pe=FAKE, slot_mapping=FAKE, kv_c_row_stride=512,
+                k_pe_row_stride=64, gamma=FAKE, positions=FAKE, cos_sin_table=FAKE,
+                max_position=100, rotate_q=1),
+           dict(num_tokens=-1)]
+    for over in bad:
+        dd = _lib.DecodeDesc.from_buffer_copy(d)
+        for k, v in over.items():
+            setattr(dd, k, v)
+        plan = ctypes.c_void_p(123)
+        st = lib.mla_plan_create(ctypes.byref(dd), ctypes.byref(plan))
+        assert st in (1, 2), (over, st)
+        assert plan.value is None, over
+    assert lib.mla_plan_run(None, None) == 1
+    lib.mla_plan_destroy(None)
