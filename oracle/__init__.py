@@ -16,6 +16,11 @@ Parity status per function (what pins each one is in ``tests/test_oracle_*.py``)
 * ``e4m3_encode``    pinned: all 65,536 bf16 patterns (raw and divided by the
                      fp32 scale 0.05) against torch's float8_e4m3fn cast where
                      |y| <= 448, plus listed ties, saturation and NaN.
+* ``e5m2_value``     pinned: the 256 codes against torch's float8_e5m2 ->
+                     float and the OCP E5M2 landmarks.
+* ``e5m2_encode``    pinned: all 65,536 bf16 patterns (raw and divided by the
+                     fp32 scales 0.05 and 3.0) against torch's float8_e5m2
+                     cast where |y| <= 57344, plus ties, saturation and NaN.
 * ``cache_write``    pinned: numpy fancy-index assignment; slot -1 leaves the
                      cache byte-identical.
 * ``decode``         pinned: torch CPU float64 scaled_dot_product_attention and
@@ -85,6 +90,8 @@ def _load():
         lib.oracle_e4m3_value_n.argtypes = [P, P, i64]
         lib.oracle_bf16_value_n.argtypes = [P, P, i64]
         lib.oracle_bf16_round_n.argtypes = [P, P, i64]
+        lib.oracle_e5m2_encode_n.argtypes = [P, P, i64]
+        lib.oracle_e5m2_value_n.argtypes = [P, P, i64]
         lib.oracle_rms_norm.argtypes = [P, i64, i64, i32, P, ctypes.c_double, P]
         lib.oracle_rms_norm.restype = None
         lib.oracle_rope_interleaved.argtypes = [P, i64, i64, i64, i32, i32, P, P, i64]
@@ -179,7 +186,8 @@ def rope_interleaved(x: np.ndarray, positions, table) -> int:
 
 def norm_rope_cache_write(kv_c, k_pe, gamma, eps: float, positions, table, slot_mapping,
                           kv_cache: np.ndarray, *, block_size: int, kv_lora_rank: int,
-                          rope_dim: int, kv_is_fp8: bool, scale: float = 1.0, q_pe=None):
+                          rope_dim: int, kv_is_fp8: bool, scale: float = 1.0, q_pe=None,
+                          fp8_format: str = "e4m3"):
     """RMSNorm of kv_c, rotary embedding of k_pe (and of ``q_pe`` [T, H, P]
     uint16, in place, when given), then the cache write of the results.  A
     token whose position is outside the table is skipped entirely (nothing
@@ -198,8 +206,29 @@ def norm_rope_cache_write(kv_c, k_pe, gamma, eps: float, positions, table, slot_
     slots[(pos < 0) | (pos >= np.asarray(table).shape[0])] = -1
     bad_slots = cache_write(normed, rot[:, 0, :], slots, kv_cache, block_size=block_size,
                             kv_lora_rank=kv_lora_rank, rope_dim=rope_dim, kv_is_fp8=kv_is_fp8,
-                            scale=scale)
+                            scale=scale, fp8_format=fp8_format)
     return bad_slots, bad_pos
+
+
+def e5m2_value(codes) -> np.ndarray:
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.empty(c.shape, np.float64)
+    _load().oracle_e5m2_value_n(_ptr(c), _ptr(out), c.size)
+    return out
+
+
+def e5m2_encode(y) -> np.ndarray:
+    v = np.ascontiguousarray(np.asarray(y, dtype=np.float32))
+    out = np.empty(v.shape, np.uint8)
+    _load().oracle_e5m2_encode_n(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def _fp8_kind(kv_is_fp8: bool, fp8_format: str) -> int:
+    """0: bf16 cache, 1: E4M3, 2: E5M2 (the C side's kv_is_fp8 argument)."""
+    if not kv_is_fp8:
+        return 0
+    return {"e4m3": 1, "e5m2": 2}[fp8_format]
 
 
 def num_kv_splits(max_seq_len: int, sm_count: int, deterministic: bool = False) -> int:
@@ -209,7 +238,7 @@ def num_kv_splits(max_seq_len: int, sm_count: int, deterministic: bool = False) 
 
 def cache_write(kv_c, k_pe, slot_mapping, kv_cache: np.ndarray, *, block_size: int,
                 kv_lora_rank: int, rope_dim: int, kv_is_fp8: bool, scale: float = 1.0,
-                block_stride: int | None = None) -> int:
+                block_stride: int | None = None, fp8_format: str = "e4m3") -> int:
     """Write tokens into ``kv_cache`` in place; returns the skipped-slot count.
 
     ``kv_c`` / ``k_pe``: bf16 (torch) or uint16 arrays [T_in, *] whose row
@@ -228,13 +257,14 @@ def cache_write(kv_c, k_pe, slot_mapping, kv_cache: np.ndarray, *, block_size: i
     return int(_load().oracle_cache_write(
         _ptr(kc), kc.strides[0] // 2, _ptr(kp), kp.strides[0] // 2, _ptr(sm), sm.size,
         kv_lora_rank, rope_dim, _ptr(kv_cache), nb, block_size, bstride,
-        int(kv_is_fp8), float(scale)))
+        _fp8_kind(kv_is_fp8, fp8_format), float(scale)))
 
 
 def decode(q, kv_cache: np.ndarray, block_table, seq_lens, *, block_size: int,
            kv_lora_rank: int, rope_dim: int, sm_scale: float, kv_is_fp8: bool = False,
            kv_scale: float = 1.0, num_kv_splits: int = 0, pairs=None,
-           block_stride: int | None = None, threads: int | None = None):
+           block_stride: int | None = None, threads: int | None = None,
+           fp8_format: str = "e4m3"):
     """fp64 decode.  Returns (o [n, R] float64, lse [n] float64).
 
     ``q``: bf16 [rows, H, R+P] (torch or uint16), last dim contiguous.
@@ -267,7 +297,8 @@ def decode(q, kv_cache: np.ndarray, block_table, seq_lens, *, block_size: int,
     so = np.empty(nthr * kv_lora_rank, np.float64)
     _load().oracle_decode(
         _ptr(qb), qb.strides[0] // 2, qb.strides[1] // 2, rows, H, _ptr(kv_cache),
-        int(kv_is_fp8), nb, block_size, bstride, kv_lora_rank, rope_dim, _ptr(bt),
+        _fp8_kind(kv_is_fp8, fp8_format), nb, block_size, bstride, kv_lora_rank, rope_dim,
+        _ptr(bt),
         bt.shape[1], _ptr(sl), sl.size, float(sm_scale), float(kv_scale),
         int(num_kv_splits), None if pr is None else _ptr(pr), n, _ptr(o), _ptr(lse),
         _ptr(ss), maxl, _ptr(so), nthr)

@@ -15,7 +15,9 @@
  *           TritonMLAMetadataBuilder.
  *   [OCP]   OCP 8-bit Floating Point Specification (OFP8), E4M3 format:
  *           bias 7, no infinities, NaN = S.1111.111, max normal 448,
- *           min normal 2^-6, min subnormal 2^-9.
+ *           min normal 2^-6, min subnormal 2^-9; E5M2 format: bias 15,
+ *           IEEE-like infinities (S.11111.00) and NaNs (S.11111.{01,10,11}),
+ *           max normal 57344, min normal 2^-14, min subnormal 2^-16.
  *
  * All floating-point work is fp64 except the one place where the pages fix
  * fp32: the fp8 quantisation step divides the fp32 input by the fp32 scale
@@ -91,6 +93,54 @@ uint8_t oracle_e4m3_encode(float y) {
   return sign | (uint8_t)code;
 }
 
+/* E5M2 code -> exact value, from the format definition [OCP]:
+ *   S.EEEEE.MM, bias 15; E == 0 is subnormal m * 2^-16; E == 31 is
+ *   infinity (M == 0) or NaN. */
+double oracle_e5m2_value(uint8_t code) {
+  int s = (code >> 7) & 1;
+  int e = (code >> 2) & 31;
+  int m = code & 3;
+  double v;
+  if (e == 31) {
+    if (m != 0) return NAN;
+    v = INFINITY;
+  } else if (e == 0) {
+    v = ldexp((double)m, -16);
+  } else {
+    v = ldexp(1.0 + m / 4.0, e - 15);
+  }
+  return s ? -v : v;
+}
+
+/* fp32 value -> E5M2 code, round to nearest with ties to even, finite
+ * overflow and infinities saturated to +-57344 (the "satfinite" reading, as
+ * for E4M3), NaN -> the positive NaN code 0x7F.  Same nearest-value search
+ * as oracle_e4m3_encode, over the 124 non-negative finite codes. */
+uint8_t oracle_e5m2_encode(float y) {
+  if (isnan(y)) return 0x7F;
+  uint8_t sign = signbit(y) ? 0x80 : 0x00;
+  double a = fabs((double)y);
+  if (a >= 57344.0) return sign | 0x7B;
+  int lo = 0, hi = 0x7B;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) / 2;
+    if (oracle_e5m2_value((uint8_t)mid) <= a)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  double dlo = a - oracle_e5m2_value((uint8_t)lo);
+  double dhi = oracle_e5m2_value((uint8_t)hi) - a;
+  int code;
+  if (dlo < dhi)
+    code = lo;
+  else if (dhi < dlo)
+    code = hi;
+  else
+    code = (lo & 1) ? hi : lo;
+  return sign | (uint8_t)code;
+}
+
 /* ------------------------------------------------------------------ */
 /* Cache write: [diff] csrc/cache_kernels.cu, concat_and_cache_mla_kernel */
 /* and its host wrapper concat_and_cache_mla.                             */
@@ -129,7 +179,8 @@ int64_t oracle_cache_write(const uint16_t *kv_c, int64_t kv_c_row_stride,
       if (kv_is_fp8) {
         float xf = (float)oracle_bf16_value(x);
         float yq = xf / scale; /* IEEE binary32 division */
-        ((uint8_t *)kv_cache)[row + i] = oracle_e4m3_encode(yq);
+        ((uint8_t *)kv_cache)[row + i] =
+            kv_is_fp8 == 2 ? oracle_e5m2_encode(yq) : oracle_e4m3_encode(yq);
       } else {
         ((uint16_t *)kv_cache)[row + i] = x;
       }
@@ -267,6 +318,9 @@ static double kv_elem(const dec_args *A, int b, int64_t j, int d) {
   if (blk < 0 || (int64_t)blk >= A->num_blocks) return 0.0;
   int64_t idx = (int64_t)blk * A->block_stride +
                 (j % A->block_size) * (int64_t)(A->R + A->P) + d;
+  if (A->kv_is_fp8 == 2)
+    return oracle_e5m2_value(((const uint8_t *)A->kv_cache)[idx]) *
+           A->kv_scale;
   if (A->kv_is_fp8)
     return oracle_e4m3_value(((const uint8_t *)A->kv_cache)[idx]) *
            A->kv_scale;
@@ -469,6 +523,12 @@ void oracle_e4m3_value_n(const uint8_t *codes, double *out, int64_t n) {
 }
 void oracle_bf16_value_n(const uint16_t *bits, double *out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_value(bits[i]);
+}
+void oracle_e5m2_encode_n(const float *y, uint8_t *out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e5m2_encode(y[i]);
+}
+void oracle_e5m2_value_n(const uint8_t *codes, double *out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e5m2_value(codes[i]);
 }
 void oracle_bf16_round_n(const double *x, uint16_t *out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_round(x[i]);
