@@ -2,8 +2,11 @@
 """Benchmark: MLA decode over a paged latent KV cache on GB300.
 
 One step = the whole hot path on one batch: the cache write of the batch's new
-tokens (mla_cache_write), the split-KV pass (mla_decode_splitkv) and the LSE
-merge (mla_decode_merge), with the split count from mla_num_kv_splits.  The
+tokens, the split-KV pass and the LSE merge, with the split count from
+mla_num_kv_splits, launched by one mla_plan_run of a plan prepared before the
+timed region (``--api calls``: the per-stage entry points mla_cache_write,
+mla_decode_splitkv and mla_decode_merge instead; the per-kernel times always
+come from a second pass through those, with an event between kernels).  The
 default workload is the DeepSeek-style per-shard decode batch (B=64, H=16,
 head 576 = 512+64, block 64, seq_lens ~ U{1024..4096}, 64 new tokens).
 
@@ -16,6 +19,8 @@ bytes / max time.
 
 ``--impl reference`` times the CPU oracle (the plain fp64 restatement of the
 method) on the host cores on a bounded sample of the same workload.
+``--op lse_merge`` times the cross-shard merge alone; ``--fused-write`` makes
+the step's write the fused RMSNorm + rotary write.
 """
 from __future__ import annotations
 
@@ -212,15 +217,32 @@ def run_ours(args, rank, world, local_rank):
 
     launches_per_step = (1 if T else 0) + 1 + (1 if S > 1 else 0)
 
+    def make_plan(q_t, bt_t, sl_t, kv_c_t, k_pe_t, slots_t):
+        """The step as one prepared plan: run() only launches the kernels."""
+        nr_args = None
+        if args.fused_write:
+            nr_args = dict(gamma=nr_gamma, eps=nr.eps, positions=nr_pos,
+                           cos_sin_table=nr_table, rotate_q=rot_q)
+        return mla.DecodePlan(q_t, cache, bt_t, sl_t, w.sm_scale, S, kv_scale=kv_scale,
+                              kv_cache_dtype="fp8" if w.kv_fp8 else None, workspace=ws,
+                              out=o, lse=lse, err_count=err, path=args.path,
+                              write=dict(kv_c=kv_c_t, k_pe=k_pe_t, slot_mapping=slots_t),
+                              norm_rope=nr_args)
+
+    plan = make_plan(q, bt, sl, kv_c, k_pe, slots) if args.api == "plan" else None
+
     def step_events():
         # One step bracketed by two events only: an event recorded between
         # two kernels would stop the next one from launching while the
         # previous one drains (programmatic dependent launch).
         e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         e[0].record(stream)
-        write(kv_c, k_pe, slots, q)
-        stage1(q, bt, sl, o, lse)
-        merge(sl, o, lse)
+        if plan is not None:
+            plan.run(stream)
+        else:
+            write(kv_c, k_pe, slots, q)
+            stage1(q, bt, sl, o, lse)
+            merge(sl, o, lse)
         e[1].record(stream)
         return e
 
@@ -293,17 +315,22 @@ def run_ours(args, rank, world, local_rank):
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_bt, h_sl, h_kvc, h_kpe, h_slots))
     d2h = h_o.numel() * h_o.element_size() + h_lse.numel() * h_lse.element_size()
 
+    e2e_plan = make_plan(d_q, d_bt, d_sl, d_kvc, d_kpe, d_slots) if args.api == "plan" else None
+
     def e2e_step():
         for dst, src in ((d_q, h_q), (d_bt, h_bt), (d_sl, h_sl), (d_kvc, h_kvc),
                          (d_kpe, h_kpe), (d_slots, h_slots)):
             dst.copy_(src, non_blocking=True)
-        write(d_kvc, d_kpe, d_slots, d_q)
-        st = lib.mla_decode(d_q.data_ptr(), d_q.stride(0), d_q.stride(1), rows, H,
-                            cache.data_ptr(), kvd, nb, bs, bstride, R, P, d_bt.data_ptr(),
-                            d_bt.stride(0), maxb, d_sl.data_ptr(), seqs, w.sm_scale,
-                            kv_scale.data_ptr(), S, ws.data_ptr(), ws.numel(), o.data_ptr(),
-                            lse.data_ptr(), err.data_ptr(), sp)
-        assert st == 0, st
+        if e2e_plan is not None:
+            e2e_plan.run(stream)
+        else:
+            write(d_kvc, d_kpe, d_slots, d_q)
+            st = lib.mla_decode(d_q.data_ptr(), d_q.stride(0), d_q.stride(1), rows, H,
+                                cache.data_ptr(), kvd, nb, bs, bstride, R, P, d_bt.data_ptr(),
+                                d_bt.stride(0), maxb, d_sl.data_ptr(), seqs, w.sm_scale,
+                                kv_scale.data_ptr(), S, ws.data_ptr(), ws.numel(),
+                                o.data_ptr(), lse.data_ptr(), err.data_ptr(), sp)
+            assert st == 0, st
         h_o.copy_(o, non_blocking=True)
         h_lse.copy_(lse, non_blocking=True)
 
@@ -361,7 +388,9 @@ def run_ours(args, rank, world, local_rank):
             "seq_lens": [int(w.seq_lens.min()), int(w.seq_lens.max())],
             "kv_tokens": int(w.seq_lens.sum()), "new_tokens": T, "num_kv_splits": S,
             "parallelism": f"replicas x{world}",
-            "write": "RMSNorm + rotary + cache write (fused)" if args.fused_write else "cache write", "l2": "flushed between steps (256 MiB write, then read back)",
+            "write": "RMSNorm + rotary + cache write (fused)" if args.fused_write else "cache write",
+            "api": "mla_plan_run (prepared plan)" if args.api == "plan"
+                   else "mla_cache_write + mla_decode_splitkv + mla_decode_merge", "l2": "flushed between steps (256 MiB write, then read back)",
         },
         "tflops": round(flops * n_units / (total_ms * 1e-3) / 1e12, 2),
         "rows_per_s": round(rows * n_units / (total_ms * 1e-3), 1),
@@ -516,6 +545,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=4,
                     help="rows per step in the --impl reference sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--api", choices=["plan", "calls"], default="plan",
+                    help="plan: one prepared mla_plan_run per step; calls: the per-stage "
+                         "entry points (mla_cache_write, mla_decode_splitkv, mla_decode_merge)")
     ap.add_argument("--fused-write", action="store_true",
                     help="the step's write also does RMSNorm of kv_c and the rotary embedding")
     ap.add_argument("--op", choices=["decode", "lse_merge"], default="decode",

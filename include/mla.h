@@ -43,9 +43,16 @@ typedef enum {
   MLA_ERR_CUDA = 4                 /* a CUDA runtime call or launch failed     */
 } mla_status;
 
-/* Element type of the cache.  "auto" in the pages' kv_cache_dtype string is
- * MLA_KV_BF16 (the cache holds the model's bf16 values unchanged). */
-typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
+/* Element type of the cache, the pages' kv_cache_dtype strings ([diff]
+ * csrc/cache_kernels.cu, concat_and_cache_mla: DISPATCH_BY_KV_CACHE_DTYPE):
+ * "auto" is MLA_KV_BF16 (the model's bf16 values unchanged), "fp8" /
+ * "fp8_e4m3" MLA_KV_FP8_E4M3 and "fp8_e5m2" MLA_KV_FP8_E5M2 (OCP formats,
+ * x / scale rounded to nearest even, finite overflow saturated). */
+typedef enum {
+  MLA_KV_BF16 = 0,
+  MLA_KV_FP8_E4M3 = 1,
+  MLA_KV_FP8_E5M2 = 2
+} mla_kv_dtype;
 
 /* Which stage-1 kernel mla_decode_ex runs.  AUTO picks the fastest kernel
  * that supports the shape; the others force one (for tests and benchmarks);
@@ -69,8 +76,10 @@ typedef enum {
  *   otherwise           row (s % bs) of block (s / bs) receives
  *                       [kv_c[t, 0:R] | k_pe[t, 0:P]].
  * bf16 cache: the bf16 bits are stored unchanged.  fp8 cache: each element
- * is E4M3(x / *scale), x / *scale an IEEE fp32 division, rounded to nearest
- * even with finite overflow saturated to +-448 (OCP E4M3, "e4m3fn").
+ * is E4M3(x / *scale) (MLA_KV_FP8_E4M3) or E5M2(x / *scale)
+ * (MLA_KV_FP8_E5M2), x / *scale an IEEE fp32 division, rounded to nearest
+ * even with finite overflow saturated to +-448 (OCP E4M3, "e4m3fn") or
+ * +-57344 (OCP E5M2).
  *
  *   kv_c            bf16 [>= num_tokens, kv_lora_rank], row stride
  *                   kv_c_row_stride (elements), unit column stride.
@@ -79,12 +88,12 @@ typedef enum {
  *   slot_mapping    int64 [num_tokens].  num_tokens may be smaller than the
  *                   rows of kv_c/k_pe (CUDA-graph padding, as in the pages).
  *   kv_lora_rank R  512 or 256.  rope_dim P: 64.
- *   kv_cache        [num_blocks, block_size, R+P] of bf16 or E4M3 bytes, the
+ *   kv_cache        [num_blocks, block_size, R+P] of bf16 or fp8 bytes, the
  *                   start of block b at element b * block_stride
  *                   (block_stride >= block_size*(R+P); block_stride*elt a
  *                   multiple of 16 bytes; kv_cache 16-byte aligned).
  *   block_size      1 .. 1024.
- *   scale           device float; read only for MLA_KV_FP8_E4M3.
+ *   scale           device float; read only for the fp8 formats.
  *   err_count       device int, may be NULL; incremented per skipped slot.
  * Duplicate slots in one call race (unspecified winner), as in the pages.
  */
@@ -113,7 +122,7 @@ mla_status mla_cache_write(const void* kv_c, int64_t kv_c_row_stride,
  * with c_i = table[p][i], s_i = table[p][P/2 + i] (any YaRN frequencies and
  * magnitude scale live in the table), computed in fp32 and rounded once to
  * bf16; then [kv_n | k_r] is stored at slot_mapping[t] exactly as
- * mla_cache_write stores [kv_c | k_pe] (bf16 copy or E4M3(x / *scale)).
+ * mla_cache_write stores [kv_c | k_pe] (bf16 copy or fp8(x / *scale)).
  * With q_pe != NULL every head of q_pe[t] is rotated the same way, in place.
  * kv_c and k_pe are not modified.
  *
@@ -181,7 +190,7 @@ size_t mla_decode_workspace_bytes(int num_rows, int num_heads,
  *
  * For row r (sequence b = r / (num_rows / num_seqs)), head h, L = seq_lens[b]:
  *   K_j = cache row of token j (page block_table[b][j / bs], row j % bs),
- *         dequantised as E4M3 value * *kv_scale for an fp8 cache;
+ *         dequantised as fp8 value * *kv_scale for an fp8 cache;
  *   s_j = sm_scale * sum_{d < R+P} q[r,h,d] K_j[d];
  *   o[r,h,:] = sum_j softmax(s)_j K_j[0:R]   (V = the kv_c part);
  *   lse[r,h] = ln sum_j exp(s_j)              (natural log, fp32).

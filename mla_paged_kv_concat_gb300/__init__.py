@@ -20,15 +20,15 @@ PyTorch supplies device memory and streams; nothing here computes the method.
 from __future__ import annotations
 
 from . import _lib
-from ._lib import (MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_PATH_AUTO, MLA_PATH_MMA_SYNC,
-                   MLA_PATH_TCGEN05, MlaError, load)
+from ._lib import (MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_KV_FP8_E5M2, MLA_PATH_AUTO,
+                   MLA_PATH_MMA_SYNC, MLA_PATH_TCGEN05, MlaError, load)
 
 __all__ = [
     "mla_cache_write", "mla_decode", "mla_decode_ex", "mla_num_kv_splits",
     "mla_decode_workspace_bytes", "mla_lse_merge", "mla_norm_rope_cache_write",
     "cache_write", "norm_rope_cache_write", "decode", "lse_merge", "DecodePlan",
     "MlaError", "load",
-    "MLA_KV_BF16", "MLA_KV_FP8_E4M3", "MLA_PATH_AUTO", "MLA_PATH_MMA_SYNC",
+    "MLA_KV_BF16", "MLA_KV_FP8_E4M3", "MLA_KV_FP8_E5M2", "MLA_PATH_AUTO", "MLA_PATH_MMA_SYNC",
     "MLA_PATH_TCGEN05",
 ]
 
@@ -83,9 +83,13 @@ def _kv_dtype(kv_cache, kv_cache_dtype: str | None) -> int:
             return MLA_KV_BF16
         if kv_cache.dtype in (torch.uint8, torch.float8_e4m3fn):
             return MLA_KV_FP8_E4M3
+        if kv_cache.dtype == torch.float8_e5m2:
+            return MLA_KV_FP8_E5M2
         raise ValueError(f"unsupported cache dtype {kv_cache.dtype}")
     if kv_cache_dtype in ("fp8", "fp8_e4m3"):
         return MLA_KV_FP8_E4M3
+    if kv_cache_dtype == "fp8_e5m2":
+        return MLA_KV_FP8_E5M2
     if kv_cache_dtype == "bf16":
         return MLA_KV_BF16
     raise ValueError(f"unsupported kv_cache_dtype {kv_cache_dtype!r}")

@@ -21,6 +21,7 @@ MLA_ERR_CUDA = 4
 
 MLA_KV_BF16 = 0
 MLA_KV_FP8_E4M3 = 1
+MLA_KV_FP8_E5M2 = 2
 
 MLA_PATH_AUTO = 0
 MLA_PATH_MMA_SYNC = 1

@@ -55,37 +55,43 @@ struct CacheWriteArgs {
 constexpr int kWarpsPerCta = 8;
 constexpr int kTokensPerWarp = 1;  // rows per warp per pass (more raised register use, not speed)
 
-// Two fp32 -> two E4M3 codes (round to nearest even, satfinite), low code
-// first.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  return static_cast<uint32_t>(
-      __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+// Cache element formats (template argument FMT of the kernel).
+constexpr int kBf16 = 0, kE4M3 = 1, kE5M2 = 2;
+
+// Two fp32 -> two fp8 codes of format FMT (round to nearest even,
+// satfinite), low code first.
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+      make_float2(lo, hi), __NV_SATFINITE, FMT == kE5M2 ? __NV_E5M2 : __NV_E4M3));
 }
 
-// E4M3 codes of RN_f32(x0 / s), RN_f32(x1 / s) (IEEE division, then RNE to
-// E4M3 with saturation), without a division in the common case.  With
+// fp8 codes of RN_f32(x0 / s), RN_f32(x1 / s) (IEEE division, then RNE to
+// E4M3 or E5M2 with saturation), without a division in the common case.  With
 // r = RN(1/s) (an IEEE division, once per thread), q = RN(x * r) is within
 // 1.5 * 2^-23 |q| of RN_f32(x / s) (three roundings of relative size at most
-// 2^-24).  E4M3 rounding is monotone in the value, so when q - 2^-22 |q| and
+// 2^-24).  fp8 rounding is monotone in the value, so when q - 2^-22 |q| and
 // q + 2^-22 |q| get the same code, so does RN_f32(x / s); otherwise the
 // quotient is within a few ulp of a boundary between two codes and the
 // division is done.  Quotients too small for the relative bound (|q| below
-// 2^-104) are all +-0 in E4M3, with the sign that both sides agree on; |q|
-// is clamped to 2^100 (every such value saturates to +-448 either way); NaN
-// quotients take the division.
+// 2^-104) are all +-0 in both formats, with the sign that both sides agree
+// on; |q| is clamped to 2^100 (every such value saturates to the largest
+// finite code either way); NaN quotients take the division.
+template <int FMT>
 __device__ __forceinline__ uint32_t quant2(float x0, float x1, float s, float r) {
   float q0 = x0 * r, q1 = x1 * r;
-  if (q0 != q0 || q1 != q1) return e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+  if (q0 != q0 || q1 != q1) return fp8x2<FMT>(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
   q0 = fminf(fmaxf(q0, -0x1p100f), 0x1p100f);
   q1 = fminf(fmaxf(q1, -0x1p100f), 0x1p100f);
   const float d0 = fabsf(q0) * 0x1p-22f, d1 = fabsf(q1) * 0x1p-22f;
-  const uint32_t lo = e4m3x2(q0 - d0, q1 - d1);
-  const uint32_t hi = e4m3x2(q0 + d0, q1 + d1);
+  const uint32_t lo = fp8x2<FMT>(q0 - d0, q1 - d1);
+  const uint32_t hi = fp8x2<FMT>(q0 + d0, q1 + d1);
   if (lo == hi) return lo;
-  return e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+  return fp8x2<FMT>(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
 }
 
-// 8 bf16 values -> 8 E4M3 bytes of x / scale (IEEE division, RNE, satfinite).
+// 8 bf16 values -> 8 fp8 bytes of x / scale (IEEE division, RNE, satfinite).
+template <int FMT>
 __device__ __forceinline__ uint2 quant8(uint4 v, float s, float r) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
   uint32_t w[2];
@@ -93,15 +99,16 @@ __device__ __forceinline__ uint2 quant8(uint4 v, float s, float r) {
   for (int k = 0; k < 2; ++k) {
     const float2 a = __bfloat1622float2(h[2 * k]);
     const float2 b = __bfloat1622float2(h[2 * k + 1]);
-    w[k] = quant2(a.x, a.y, s, r) | (quant2(b.x, b.y, s, r) << 16);
+    w[k] = quant2<FMT>(a.x, a.y, s, r) | (quant2<FMT>(b.x, b.y, s, r) << 16);
   }
   return make_uint2(w[0], w[1]);
 }
 
+template <int FMT>
 __device__ __forceinline__ uint8_t quant1(uint16_t bits, float s) {
   float x = __bfloat162float(__ushort_as_bfloat16(bits));
-  return static_cast<uint8_t>(
-      __nv_cvt_float_to_fp8(__fdiv_rn(x, s), __NV_SATFINITE, __NV_E4M3));
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fdiv_rn(x, s), __NV_SATFINITE,
+                                                    FMT == kE5M2 ? __NV_E5M2 : __NV_E4M3));
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -134,9 +141,10 @@ __device__ __forceinline__ uint4 rope8(uint4 x, float4 c, float4 s) {
 // VEC: every source row and destination row starts on a 16-byte boundary, so
 // rows move as 16-byte chunks (8 elements); otherwise element by element.
 // NR: the fused RMSNorm + rotary variant (VEC layout, P = 64 only).
-template <bool FP8, bool VEC, bool NR = false>
+template <int FMT, bool VEC, bool NR = false>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, NR ? 3 : 1)
     cache_write_kernel(const CacheWriteArgs a) {
+  constexpr bool FP8 = FMT != kBf16;
   // The decode kernels that follow wait for this grid's completion before
   // they read anything; letting them launch now hides their launch latency.
   griddep_launch_dependents();
@@ -261,7 +269,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NR ? 3 : 1)
           if (c >= nc + np) break;
           if constexpr (FP8) {
             uint8_t* dst = static_cast<uint8_t*>(a.cache) + dst_elem;
-            reinterpret_cast<uint2*>(dst)[c] = quant8(v[j][k], s, r);
+            reinterpret_cast<uint2*>(dst)[c] = quant8<FMT>(v[j][k], s, r);
           } else {
             uint16_t* dst = static_cast<uint16_t*>(a.cache) + dst_elem;
             reinterpret_cast<uint4*>(dst)[c] = v[j][k];
@@ -284,7 +292,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NR ? 3 : 1)
         for (int i = lane; i < D; i += 32) {
           const uint16_t x = (i < a.R) ? src_c[i] : src_p[i - a.R];
           if constexpr (FP8)
-            static_cast<uint8_t*>(a.cache)[dst_elem + i] = quant1(x, s);
+            static_cast<uint8_t*>(a.cache)[dst_elem + i] = quant1<FMT>(x, s);
           else
             static_cast<uint16_t*>(a.cache)[dst_elem + i] = x;
         }
@@ -299,10 +307,11 @@ cudaError_t launch_cache_write(const void* kv_c, int64_t kv_c_stride,
                                const void* k_pe, int64_t k_pe_stride,
                                const int64_t* slot_mapping, int num_tokens,
                                int R, int P, void* cache, int num_blocks,
-                               int block_size, int64_t block_stride, bool fp8,
+                               int block_size, int64_t block_stride, int fmt,
                                const float* scale, int* err_count,
                                cudaStream_t stream) {
   if (num_tokens == 0) return cudaSuccess;
+  const bool fp8 = fmt != kBf16;
   CacheWriteArgs a;
   a.kv_c = static_cast<const uint16_t*>(kv_c);
   a.kv_c_stride = kv_c_stride;
@@ -343,16 +352,21 @@ cudaError_t launch_cache_write(const void* kv_c, int64_t kv_c_stride,
   const int64_t need = (static_cast<int64_t>(num_tokens) + per_cta - 1) / per_cta;
   const dim3 grid(static_cast<unsigned>(need < 8 * sms ? need : 8 * sms));
   const dim3 block(kWarpsPerCta * 32);
-  if (fp8) {
+  if (fmt == kE4M3) {
     if (vec)
-      cache_write_kernel<true, true><<<grid, block, 0, stream>>>(a);
+      cache_write_kernel<kE4M3, true><<<grid, block, 0, stream>>>(a);
     else
-      cache_write_kernel<true, false><<<grid, block, 0, stream>>>(a);
+      cache_write_kernel<kE4M3, false><<<grid, block, 0, stream>>>(a);
+  } else if (fmt == kE5M2) {
+    if (vec)
+      cache_write_kernel<kE5M2, true><<<grid, block, 0, stream>>>(a);
+    else
+      cache_write_kernel<kE5M2, false><<<grid, block, 0, stream>>>(a);
   } else {
     if (vec)
-      cache_write_kernel<false, true><<<grid, block, 0, stream>>>(a);
+      cache_write_kernel<kBf16, true><<<grid, block, 0, stream>>>(a);
     else
-      cache_write_kernel<false, false><<<grid, block, 0, stream>>>(a);
+      cache_write_kernel<kBf16, false><<<grid, block, 0, stream>>>(a);
   }
   return cudaGetLastError();
 }
@@ -360,7 +374,7 @@ cudaError_t launch_cache_write(const void* kv_c, int64_t kv_c_stride,
 cudaError_t launch_norm_rope_cache_write(const void* kv_c, int64_t kv_c_stride, const void* k_pe,
                                          int64_t k_pe_stride, const int64_t* slot_mapping,
                                          int num_tokens, int R, void* cache, int num_blocks,
-                                         int block_size, int64_t block_stride, bool fp8,
+                                         int block_size, int64_t block_stride, int fmt,
                                          const float* scale, const void* gamma, float eps,
                                          const int64_t* positions, const float* table,
                                          int64_t max_position, void* q_pe,
@@ -397,10 +411,12 @@ cudaError_t launch_norm_rope_cache_write(const void* kv_c, int64_t kv_c_stride, 
   const int64_t need = (static_cast<int64_t>(num_tokens) + kWarpsPerCta - 1) / kWarpsPerCta;
   const dim3 grid(static_cast<unsigned>(need < 8 * sms ? need : 8 * sms));
   const dim3 block(kWarpsPerCta * 32);
-  if (fp8)
-    cache_write_kernel<true, true, true><<<grid, block, 0, stream>>>(a);
+  if (fmt == kE4M3)
+    cache_write_kernel<kE4M3, true, true><<<grid, block, 0, stream>>>(a);
+  else if (fmt == kE5M2)
+    cache_write_kernel<kE5M2, true, true><<<grid, block, 0, stream>>>(a);
   else
-    cache_write_kernel<false, true, true><<<grid, block, 0, stream>>>(a);
+    cache_write_kernel<kBf16, true, true><<<grid, block, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

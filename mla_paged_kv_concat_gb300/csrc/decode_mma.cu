@@ -33,7 +33,7 @@
 //     sums are exchanged through shared memory; P (bf16) goes to shared
 //     memory; O += P.V with each warp owning a quarter of the latent columns,
 //     accumulators in registers.
-//   * fp8 (E4M3) tiles are converted exactly to bf16 in shared memory by the
+//   * fp8 (E4M3 or E5M2) tiles are converted exactly to bf16 in shared memory by the
 //     consumers; the dequantisation scale is folded into the score scale and
 //     the final output scale.
 #include <cuda_bf16.h>
@@ -83,15 +83,16 @@ struct MmaCfg {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// 16 E4M3 bytes -> 16 bf16 values (exact: every E4M3 value is a bf16 value).
-__device__ __forceinline__ void e4m3x16_to_bf16(uint4 raw, uint4& lo,
-                                                uint4& hi) {
+// 16 fp8 bytes (E4M3, or E5M2 when e5m2) -> 16 bf16 values (exact: every
+// E4M3 and every E5M2 value is a bf16 value).
+__device__ __forceinline__ void fp8x16_to_bf16(uint4 raw, bool e5m2, uint4& lo,
+                                               uint4& hi) {
   const uint16_t* b = reinterpret_cast<const uint16_t*>(&raw);
   uint32_t out[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-        static_cast<__nv_fp8x2_storage_t>(b[k]), __NV_E4M3);
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(b[k]),
+                                               e5m2 ? __NV_E5M2 : __NV_E4M3);
     float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
     out[k] = pack_bf16x2(f.x, f.y);
   }
@@ -457,9 +458,9 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
           const int c = idx / (kBN * 4), r = (idx >> 2) % kBN, kq = idx & 3;
           uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
           if (r < valid)
-            e4m3x16_to_bf16(
+            fp8x16_to_bf16(
                 *reinterpret_cast<const uint4*>(raw + c * (kBN * 64) + r * 64 + kq * 16),
-                lo, hi);
+                p.kv_e5m2 != 0, lo, hi);
           uint8_t* dst = s_conv + c * (kBN * 128);
           *reinterpret_cast<uint4*>(dst + sw128(r, 2 * kq)) = lo;
           *reinterpret_cast<uint4*>(dst + sw128(r, 2 * kq + 1)) = hi;

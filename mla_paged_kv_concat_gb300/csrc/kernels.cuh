@@ -26,6 +26,7 @@ struct DecodeParams {
   int block_size, num_blocks;
   float sm_scale;
   const float* kv_scale;  // device; fp8 cache only (else nullptr)
+  int kv_e5m2;            // fp8 cache holds E5M2 codes (else E4M3)
   int num_splits;
   float* ws_o;    // [rows][S][H][R] fp32 partial outputs (S > 1)
   float* ws_lse;  // [rows][S][H] fp32 partial lse (S > 1)
@@ -54,11 +55,12 @@ inline cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 b
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// fmt: cache element format, the mla_kv_dtype value (0 bf16, 1 E4M3, 2 E5M2).
 cudaError_t launch_cache_write(const void* kv_c, int64_t kv_c_stride,
                                const void* k_pe, int64_t k_pe_stride,
                                const int64_t* slot_mapping, int num_tokens,
                                int R, int P, void* cache, int num_blocks,
-                               int block_size, int64_t block_stride, bool fp8,
+                               int block_size, int64_t block_stride, int fmt,
                                const float* scale, int* err_count,
                                cudaStream_t stream);
 
@@ -68,7 +70,7 @@ cudaError_t launch_cache_write(const void* kv_c, int64_t kv_c_stride,
 cudaError_t launch_norm_rope_cache_write(const void* kv_c, int64_t kv_c_stride, const void* k_pe,
                                          int64_t k_pe_stride, const int64_t* slot_mapping,
                                          int num_tokens, int R, void* cache, int num_blocks,
-                                         int block_size, int64_t block_stride, bool fp8,
+                                         int block_size, int64_t block_stride, int fmt,
                                          const float* scale, const void* gamma, float eps,
                                          const int64_t* positions, const float* table,
                                          int64_t max_position, void* q_pe,

@@ -23,6 +23,10 @@ mla_status cuda_fail(cudaError_t e) {
   return MLA_ERR_CUDA;
 }
 
+bool valid_kv_dtype(mla_kv_dtype t) {
+  return t == MLA_KV_BF16 || t == MLA_KV_FP8_E4M3 || t == MLA_KV_FP8_E5M2;
+}
+
 bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
@@ -173,12 +177,11 @@ mla_status cache_write_impl(const void* kv_c, int64_t kv_c_row_stride, const voi
   if (num_tokens < 0 || kv_lora_rank <= 0 || rope_dim <= 0 ||
       num_blocks <= 0 || block_size <= 0 || block_size > 1024)
     return MLA_ERR_INVALID_ARG;
-  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3)
-    return MLA_ERR_INVALID_ARG;
+  if (!valid_kv_dtype(kv_dtype)) return MLA_ERR_INVALID_ARG;
   if (!supported_latent(kv_lora_rank, rope_dim)) return MLA_ERR_UNSUPPORTED;
   if (num_tokens == 0) return MLA_OK;
   if (!kv_c || !k_pe || !slot_mapping || !kv_cache) return MLA_ERR_INVALID_ARG;
-  const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  const bool fp8 = kv_dtype != MLA_KV_BF16;
   if (fp8 && !scale) return MLA_ERR_INVALID_ARG;
   if (kv_c_row_stride < kv_lora_rank || k_pe_row_stride < rope_dim)
     return MLA_ERR_INVALID_ARG;
@@ -191,7 +194,7 @@ mla_status cache_write_impl(const void* kv_c, int64_t kv_c_row_stride, const voi
   cudaError_t e = mla::launch_cache_write(
       kv_c, kv_c_row_stride, k_pe, k_pe_row_stride, slot_mapping, num_tokens,
       kv_lora_rank, rope_dim, kv_cache, num_blocks, block_size, block_stride,
-      fp8, scale, err_count, static_cast<cudaStream_t>(stream));
+      static_cast<int>(kv_dtype), scale, err_count, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 
@@ -208,13 +211,13 @@ mla_status nr_write_impl(const void* kv_c, int64_t kv_c_row_stride, const void* 
   if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || block_size > 1024 ||
       max_position <= 0 || !(eps >= 0.f))
     return MLA_ERR_INVALID_ARG;
-  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (!valid_kv_dtype(kv_dtype)) return MLA_ERR_INVALID_ARG;
   if (rope_dim != 64 || (kv_lora_rank != 512 && kv_lora_rank != 256))
     return MLA_ERR_UNSUPPORTED;
   if (num_tokens == 0) return MLA_OK;
   if (!kv_c || !k_pe || !slot_mapping || !kv_cache || !gamma || !positions || !cos_sin_table)
     return MLA_ERR_INVALID_ARG;
-  const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  const bool fp8 = kv_dtype != MLA_KV_BF16;
   if (fp8 && !scale) return MLA_ERR_INVALID_ARG;
   if (kv_c_row_stride < kv_lora_rank || k_pe_row_stride < rope_dim ||
       kv_c_row_stride % 8 != 0 || k_pe_row_stride % 8 != 0 || !aligned16(kv_c) ||
@@ -233,7 +236,8 @@ mla_status nr_write_impl(const void* kv_c, int64_t kv_c_row_stride, const void* 
   if (!do_launch) return MLA_OK;
   cudaError_t e = mla::launch_norm_rope_cache_write(
       kv_c, kv_c_row_stride, k_pe, k_pe_row_stride, slot_mapping, num_tokens, kv_lora_rank,
-      kv_cache, num_blocks, block_size, block_stride, fp8, scale, gamma, eps, positions,
+      kv_cache, num_blocks, block_size, block_stride, static_cast<int>(kv_dtype), scale, gamma,
+      eps, positions,
       cos_sin_table, max_position, q_pe, q_pe_row_stride, q_pe_head_stride,
       q_pe != nullptr ? q_pe_heads : 0, err_count, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
@@ -299,8 +303,7 @@ mla_status prepare_decode(const void* q, int64_t q_row_stride,
       num_blocks <= 0 || block_size <= 0 || max_blocks_per_seq < 1 ||
       num_kv_splits < 1 || num_kv_splits > 65535)
     return MLA_ERR_INVALID_ARG;
-  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3)
-    return MLA_ERR_INVALID_ARG;
+  if (!valid_kv_dtype(kv_dtype)) return MLA_ERR_INVALID_ARG;
   if (path != MLA_PATH_AUTO && path != MLA_PATH_MMA_SYNC &&
       path != MLA_PATH_TCGEN05)
     return MLA_ERR_INVALID_ARG;
@@ -310,7 +313,7 @@ mla_status prepare_decode(const void* q, int64_t q_row_stride,
   if (num_seqs == 0 || num_rows % num_seqs != 0 || num_seqs > 65535)
     return MLA_ERR_INVALID_ARG;
   const int D = kv_lora_rank + rope_dim;
-  const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  const bool fp8 = kv_dtype != MLA_KV_BF16;
   const size_t elt = fp8 ? 1 : 2;
   // ---- pointers, strides, alignment
   if (!q || !kv_cache || !block_table || !seq_lens || !o || !lse)
@@ -368,6 +371,7 @@ mla_status prepare_decode(const void* q, int64_t q_row_stride,
   p->num_blocks = num_blocks;
   p->sm_scale = sm_scale;
   p->kv_scale = fp8 ? kv_scale : nullptr;
+  p->kv_e5m2 = kv_dtype == MLA_KV_FP8_E5M2 ? 1 : 0;
   p->num_splits = num_kv_splits;
   const size_t n_o = static_cast<size_t>(num_rows) * num_heads * num_kv_splits *
                      kv_lora_rank;
@@ -470,7 +474,7 @@ mla_status mla_decode_splitkv(const void* q, int64_t q_row_stride,
       sm_scale, kv_scale, num_kv_splits, workspace, workspace_bytes, o, lse,
       err_count, path, &p);
   if (st != MLA_OK || num_rows == 0) return st;
-  return run_stage1(p, kv_cache, kv_dtype == MLA_KV_FP8_E4M3, kv_lora_rank,
+  return run_stage1(p, kv_cache, kv_dtype != MLA_KV_BF16, kv_lora_rank,
                     block_size, num_blocks, block_stride, path,
                     static_cast<cudaStream_t>(stream));
 }
@@ -556,7 +560,7 @@ mla_status mla_decode_ex(const void* q, int64_t q_row_stride,
       err_count, path, &p);
   if (st != MLA_OK || num_rows == 0) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = run_stage1(p, kv_cache, kv_dtype == MLA_KV_FP8_E4M3, kv_lora_rank,
+  st = run_stage1(p, kv_cache, kv_dtype != MLA_KV_BF16, kv_lora_rank,
                   block_size, num_blocks, block_stride, path, s);
   if (st != MLA_OK) return st;
   if (num_kv_splits > 1) {
@@ -653,7 +657,7 @@ mla_status mla_plan_create(const mla_decode_desc* desc, mla_decode_plan** plan) 
   pl->d = d;
   pl->has_stage1 = d.num_rows > 0;
   if (pl->has_stage1) {
-    st = build_stage1(p, d.kv_cache, d.kv_dtype == MLA_KV_FP8_E4M3, d.kv_lora_rank,
+    st = build_stage1(p, d.kv_cache, d.kv_dtype != MLA_KV_BF16, d.kv_lora_rank,
                       d.block_size, d.num_blocks, d.block_stride, d.path, &pl->s1);
     if (st != MLA_OK) {
       delete pl;

@@ -70,7 +70,8 @@ def _decode_args(**over):
     (dict(H=0), 1), (dict(H=129), 1), (dict(S=0), 1), (dict(rows=3), 1),
     (dict(R=384), 2), (dict(P=32), 2), (dict(bs=48), 2), (dict(bs=8), 2),
     (dict(bstride=64 * 576 - 8), 1), (dict(q=FAKE + 2), 1), (dict(qhs=500), 1),
-    (dict(kvd=1, kvs=None), 1), (dict(kvd=7), 1), (dict(path=9), 1),
+    (dict(kvd=1, kvs=None), 1), (dict(kvd=2, kvs=None), 1), (dict(kvd=7), 1),
+    (dict(kvd=3), 1), (dict(path=9), 1),
     (dict(wsb=100), 3), (dict(ws=None), 1), (dict(ws=FAKE + 4), 1),
     (dict(bts=2), 1),
 ])
@@ -89,6 +90,7 @@ def _write_args(**over):
 @pytest.mark.parametrize("over,code", [
     (dict(kv_c=None), 1), (dict(slots=None), 1), (dict(cache=None), 1),
     (dict(T=-1), 1), (dict(R=100), 2), (dict(kvd=1, scale=None), 1),
+    (dict(kvd=2, scale=None), 1), (dict(kvd=3, scale=FAKE), 1),
     (dict(bstride=100), 1), (dict(cache=FAKE + 8), 1), (dict(kcs=10), 1),
     (dict(nb=0), 1), (dict(bs=0), 1),
 ])
