@@ -28,9 +28,10 @@ namespace mla {
 namespace {
 
 constexpr int kMergeWarps = 8;
+constexpr int kInFlight = 2;  // partial rows loaded together per warp
 
 template <int R>
-__global__ void __launch_bounds__(kMergeWarps * 32)
+__global__ void __launch_bounds__(kMergeWarps * 32, 3)
     merge_kernel(const DecodeParams p) {
   constexpr int NV = R / 128;  // float4 groups per lane
   griddep_wait();              // stage 1's partials are complete and visible
@@ -62,23 +63,24 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   for (int k = 0; k < NV; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;  // this lane's slots; summed over the warp at the end
   for (int c = 0; c < S; c += 32) {
-    // Lane j holds the weight of slot c + j; the partial rows of up to four
-    // non-empty slots are loaded together, then added in slot order.
+    // Lane j holds the weight of slot c + j; the partial rows of up to
+    // kInFlight non-empty slots are loaded together, then added in slot
+    // order (few rows per warp, many warps per SM).
     const int s = c + lane;
     const float ls = s < S ? p.ws_lse[rec0 + static_cast<int64_t>(s) * H] : -INFINITY;
     const float w = ls == -INFINITY ? 0.f : __expf(ls - M);
     den += w;
     uint32_t mask = __ballot_sync(0xffffffffu, w != 0.f);
     while (mask) {
-      int js[4];
+      int js[kInFlight];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kInFlight; ++u) {
         js[u] = mask ? __ffs(mask) - 1 : -1;
         mask &= mask ? mask - 1 : 0u;
       }
-      float4 v[4][NV];
+      float4 v[kInFlight][NV];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kInFlight; ++u) {
         if (js[u] < 0) continue;
         const float4* src = reinterpret_cast<const float4*>(
             p.ws_o + (rec0 + static_cast<int64_t>(c + js[u]) * H) * R);
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
         for (int k = 0; k < NV; ++k) v[u][k] = src[k * 32 + lane];
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kInFlight; ++u) {
         if (js[u] < 0) continue;
         const float wj = __shfl_sync(0xffffffffu, w, js[u]);
 #pragma unroll
