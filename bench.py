@@ -126,6 +126,25 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- multi-rank host logic
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over all ranks (x itself without a process
+    group).  The timed region of the slowest replica sets the job's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_step: int, steps: int, world: int, total_ms: float) -> float:
+    """Whole-job GB/s: the bytes every replica processed over the slowest
+    replica's time (replicas: each of the `world` ranks runs its own batch)."""
+    return bytes_per_step * steps * world / (total_ms * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -292,16 +311,12 @@ def run_ours(args, rank, world, local_rank):
     t_s1 = [e[1].elapsed_time(e[2]) for e in kevs]
     t_merge = [e[2].elapsed_time(e[3]) for e in kevs]
     t_step = [e[0].elapsed_time(e[1]) for e in evs]
-    total_ms = float(np.sum(t_step))
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(np.sum(t_step)), dev)
     ms_step = total_ms / args.steps
     kv_bytes = w.kv_bytes()
     flops = w.flops()
     n_units = world * args.steps
-    value = kv_bytes * n_units / (total_ms * 1e-3) / 1e9
+    value = job_throughput(kv_bytes, args.steps, world, total_ms)
 
     # ---- e2e through the C ABI with host buffers (pinned), copies timed.
     # The step's inputs sit in one pinned host block and go over in one
@@ -370,12 +385,8 @@ def run_ours(args, rank, world, local_rank):
         b.record(stream)
         e2e_ms.append((a, b))
     torch.cuda.synchronize(dev)
-    e2e_total = float(sum(a.elapsed_time(b) for a, b in e2e_ms))
-    if dist is not None:
-        t = torch.tensor([e2e_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_value = kv_bytes * n_units / (e2e_total * 1e-3) / 1e9
+    e2e_total = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in e2e_ms)), dev)
+    e2e_value = job_throughput(kv_bytes, args.steps, world, e2e_total)
     if int(err.item()) != 0:
         print(f"warning: device error counter {int(err.item())}", file=sys.stderr)
 
