@@ -126,16 +126,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map,
       : "memory");
 }
 
-// Fetches the same box as tma_load_3d into L2 only (no shared memory, no
-// barrier): the later load of that box then comes from L2.
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1,
-                                                   int c2) {
-  asm volatile(
-      "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map),
-      "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- ldmatrix
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0,
                                         uint32_t& r1, uint32_t& r2,
@@ -206,8 +196,4 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
                    smem_u32(bar))
                : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
 }  // namespace mla

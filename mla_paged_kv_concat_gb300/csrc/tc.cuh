@@ -66,19 +66,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-// ------------------------------------------------------------ MMA
-// D[tmem] (+)= A[smem] * B[smem], issued by one thread.
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc,
-                                       uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Arrive on `bar` once every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {
@@ -119,16 +106,6 @@ __device__ __forceinline__ void st_32x32b_x32(uint32_t taddr, const uint32_t (&r
       "r"(r[31])
       : "memory");
 }
-// 32 lanes x 16 consecutive 32-bit columns (see ld_32x32b_x32).
-__device__ __forceinline__ void ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
-        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
 __device__ __forceinline__ void st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -168,18 +145,6 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c,
-                                              float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a),
-               "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-// Arrive (release, cluster scope) on an mbarrier in another CTA's shared memory.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile(
-      "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-      : "memory");
-}
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -209,17 +174,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 namespace mla {
 namespace tc {
 
-// 16-byte store into another CTA's shared memory that completes `bytes` of
-// the transaction count of the mbarrier at `cluster_bar` (also in that CTA)
-// once the data is there: no fence on either side.
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b,
-                                            float c, float d, uint32_t cluster_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], "
-      "{%1, %2, %3, %4}, [%5];" ::"r"(cluster_addr),
-      "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
-      : "memory");
-}
 __device__ __forceinline__ void st_async_v4u(uint32_t cluster_addr, uint32_t a, uint32_t b,
                                              uint32_t c, uint32_t d, uint32_t cluster_bar) {
   asm volatile(
@@ -254,20 +208,6 @@ __device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity
 
 namespace mla {
 namespace tc {
-
-// Copies `bytes` (a multiple of 16) from this CTA's shared memory to the
-// shared memory of another CTA of the cluster (`dst` and `bar` are cluster
-// addresses there); the copy completes `bytes` of the transaction count of
-// that CTA's mbarrier `bar`.  The source must be made visible to the async
-// proxy (fence_proxy_async_smem) by the threads that wrote it.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
-                                                  uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes "
-      "[%0], [%1], %2, [%3];" ::"r"(dst),
-      "r"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 
 // D[tmem] (+)= A[tmem] * B[smem]: A is M lanes x K columns of packed 16-bit
 // pairs (lane m, column k/2, low half = even k); issued by one thread.
