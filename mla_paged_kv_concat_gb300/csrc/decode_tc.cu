@@ -114,11 +114,12 @@ __device__ __forceinline__ uint32_t xoff(uint32_t r, uint32_t c, uint32_t row_by
 
 // One unit of work of a CTA pair: tokens [start, end) of sequence b for the
 // 128-vector block g, whose result goes to split slot `slot` (or straight to
-// o / lse when `direct`).  `mark_lo..mark_hi` are slots this segment marks
-// unused (lse = -inf): fused splits in grid mode, or the slots a unit's
-// partition leaves free (written by its first segment) in persistent mode.
+// o / lse when `direct`).  `mark_lo..mark_hi` and `mark2_lo..mark2_hi` are
+// slots this segment marks unused (lse = -inf): fused splits in grid mode,
+// or the slots the persistent partition leaves free (written by the first
+// segment of a chunk).
 struct TcSeg {
-  int b, g, start, end, slot, mark_lo, mark_hi;
+  int b, g, start, end, slot, mark_lo, mark_hi, mark2_lo, mark2_hi;
   bool direct;
 };
 
@@ -175,6 +176,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   // boundaries (the same walk as the warp-MMA kernel's).  Grid: one segment
   // per pair, split_group consecutive splits of one unit.
   int units = 0, C = 1, lo = 0, hi = 0, cidx = 0;
+  // Sequences with several 128-vector blocks are cut into chunks of CH
+  // tiles and listed chunk by chunk, all blocks of a chunk side by side, so
+  // that the pairs holding the blocks of one chunk stream the same KV tiles
+  // at about the same time and L2 serves all but the first reader.  A chunk
+  // of one block spans at most SPC pairs and owns SPC split slots.
+  int CH = 1 << 30, SPC = 1;
   TcSeg gseg{};
   int nseg = 0;
   if (persistent) {
@@ -214,6 +221,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     C = max(max(cdiv(total, npairs), cdiv(s_max, max(S - 1, 1))), 1);
     lo = cidx * C;
     hi = min(total, lo + C);
+    SPC = S;  // one block per sequence: one chunk, slot = pair - first pair
+    if (qblocks > 1) {
+      // smallest m with (chunks) x (slots per chunk) <= S; m = cdiv(s_max, C)
+      // (one chunk) always qualifies because C >= cdiv(s_max, S - 1)
+      for (int m = 1;; ++m) {
+        const int J = cdiv(s_max, C * m);
+        if (J * (m + 1) <= S || J == 1) {
+          CH = C * m;
+          SPC = m + 1;
+          break;
+        }
+      }
+    }
     if (lo >= hi) return;  // both CTAs of the pair leave together
   } else {
     const int b = blockIdx.z, ysplit = blockIdx.y;
@@ -234,6 +254,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     gseg.slot = s0;
     gseg.mark_lo = s0 + 1;
     gseg.mark_hi = s1;
+    gseg.mark2_lo = gseg.mark2_hi = 0;
     gseg.direct = S == 1;
     if (gseg.start >= gseg.end) {
       // Both CTAs of the pair take this branch together.
@@ -260,50 +281,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   }
   // Walks this pair's segments in order, calling f(seg, index, first tile
   // (a running count over the pair's segments), next segment or nullptr).
-  auto make_seg = [&](int u, TcSeg& s) {
-    const int t_lo = max(lo, pre[u]) - pre[u], t_hi = min(hi, pre[u + 1]) - pre[u];
-    s.b = u / qblocks;
-    s.g = u - s.b * qblocks;
-    const int L = lens[s.b] & ~kClampedBit;
-    s.start = t_lo * TBN;
-    s.end = min(L, t_hi * TBN);
-    const int cf = pre[u] / C;
-    s.slot = cidx - cf;
-    s.mark_lo = s.slot == 0 ? (pre[u + 1] - 1) / C - cf + 1 : S;
-    s.mark_hi = S;
+  // The pair's segment that starts at tile t of the list (lo <= t < hi);
+  // returns the list position where the next segment starts.
+  auto seg_at = [&](int t, TcSeg& s) -> int {
+    int a = 0, z = p.num_seqs - 1;  // sequence b: the last with pre[b * qblocks] <= t
+    while (a < z) {
+      const int m = (a + z + 1) >> 1;
+      if (pre[m * qblocks] <= t) a = m; else z = m - 1;
+    }
+    const int b = a;
+    const int Ob = pre[b * qblocks];
+    const int Tb = pre[b * qblocks + 1] - Ob;  // tiles of the sequence
+    const int Jb = cdiv(Tb, CH);
+    const int64_t span = static_cast<int64_t>(qblocks) * CH;  // list tiles of a full chunk
+    const int x = t - Ob;
+    const int j = static_cast<int>(min(static_cast<int64_t>(x) / span, static_cast<int64_t>(Jb - 1)));
+    const int len = j == Jb - 1 ? Tb - (Jb - 1) * CH : CH;  // tiles of chunk j
+    const int y = x - static_cast<int>(j * span);
+    const int g = y / len;
+    const int in = y - g * len;  // tile of the chunk where this segment starts
+    const int vstart = Ob + static_cast<int>(j * span) + g * len;
+    const int vend = vstart + len;
+    const int seg_end = min(hi, vend);
+    const int L = lens[b] & ~kClampedBit;
+    s.b = b;
+    s.g = g;
+    s.start = (j * CH + in) * TBN;
+    s.end = min(L, (j * CH + in + (seg_end - t)) * TBN);
+    const int cf = vstart / C;  // the pair where chunk j of block g begins
+    s.slot = j * SPC + (cidx - cf);
+    const bool first = cidx == cf;
+    s.mark_lo = first ? j * SPC + ((vend - 1) / C - cf + 1) : 0;
+    s.mark_hi = first ? (j + 1) * SPC : 0;
+    s.mark2_lo = first && j == 0 ? Jb * SPC : 0;  // slots past the last chunk
+    s.mark2_hi = first && j == 0 ? S : 0;
     s.direct = false;
-  };
-  // first unit at or after u that has tiles in [lo, hi), or -1
-  auto next_unit = [&](int u) {
-    for (; u < units && pre[u] < hi; ++u)
-      if (min(hi, pre[u + 1]) > max(lo, pre[u])) return u;
-    return -1;
+    return seg_end;
   };
   auto for_each_seg = [&](auto&& f) {
     if (!persistent) {
       if (nseg) f(gseg, 0, 0, static_cast<const TcSeg*>(nullptr));
       return;
     }
-    int a = 0, z = units;  // first unit with pre[u + 1] > lo
-    while (a < z) {
-      const int m = (a + z) >> 1;
-      if (pre[m + 1] > lo) z = m; else a = m + 1;
-    }
-    int u = next_unit(a);
-    if (u < 0) return;
+    if (lo >= hi) return;
     TcSeg cur, nxt;
-    make_seg(u, cur);
+    int t_next = seg_at(lo, cur);
     for (int k = 0, n0 = 0;; ++k) {
-      const int u2 = next_unit(u + 1);
-      if (u2 >= 0) make_seg(u2, nxt);
+      const bool more = t_next < hi;
+      int t_after = hi;
+      if (more) t_after = seg_at(t_next, nxt);
       if (cur.slot == 0 && cur.g == 0 && (lens[cur.b] & kClampedBit) && threadIdx.x == 0 &&
           rank == 0 && p.err_count)
         atomicAdd(p.err_count, 1);  // seq_len beyond the block table, once per sequence
-      if (!f(cur, k, n0, u2 >= 0 ? &nxt : static_cast<const TcSeg*>(nullptr))) return;
-      if (u2 < 0) return;
+      if (!f(cur, k, n0, more ? &nxt : static_cast<const TcSeg*>(nullptr))) return;
+      if (!more) return;
       n0 += cdiv(cur.end - cur.start, TBN);
-      u = u2;
       cur = nxt;
+      t_next = t_after;
     }
   };
 
@@ -869,6 +903,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         } else {
           p.ws_lse[rec] = lse;
           for (int s = sg.mark_lo; s < sg.mark_hi; ++s)
+            p.ws_lse[(static_cast<int64_t>(row) * S + s) * H + hd] = -INFINITY;
+          for (int s = sg.mark2_lo; s < sg.mark2_hi; ++s)
             p.ws_lse[(static_cast<int64_t>(row) * S + s) * H + hd] = -INFINITY;
         }
       }
