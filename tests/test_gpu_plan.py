@@ -169,3 +169,27 @@ def test_plan_graph_replay_over_new_contents(cuda_dev, H, fused, pair):
             assert d.cache_numpy().tobytes() == cache_ref.tobytes()
         assert_close(plan.out, plan.lse, o_ref, lse_ref, what=f"replay H={H} L={w.seq_lens}")
     plan.close()
+
+
+@pytest.mark.parametrize("name,npairs", [("per_shard", 128), ("full_head", 32)])
+def test_benchmark_configuration_through_a_plan(cuda_dev, name, npairs):
+    """The benchmark's step as it times it: one plan over the resident
+    tensors (write of the new tokens, stage 1 at the rule's split count,
+    merge), run once; the cache compared byte for byte and sampled (row, head)
+    outputs against the oracle."""
+    from _helpers import sample_pairs
+    w = W.make(name)
+    d = _device(w)
+    S = mla.mla_num_kv_splits(w.max_seq_len, sm_count())
+    plan = mla.DecodePlan(d.q, d.cache, d.block_table, d.seq_lens, w.sm_scale, S,
+                          err_count=d.err,
+                          write=dict(kv_c=d.kv_c, k_pe=d.k_pe, slot_mapping=d.slot_mapping))
+    o, lse = plan.run()
+    torch.cuda.synchronize()
+    plan.close()
+    assert int(d.err.item()) == 0
+    cache = oracle_cache(w)
+    assert d.cache_numpy().tobytes() == cache.tobytes()
+    pairs = sample_pairs(w, npairs, seed=11)
+    o_ref, lse_ref = oracle_decode(w, cache, pairs=pairs)
+    assert_close(o, lse, o_ref, lse_ref, pairs=pairs, what=f"{name} through a plan")
