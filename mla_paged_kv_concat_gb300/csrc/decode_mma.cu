@@ -110,19 +110,30 @@ constexpr int kClampedBit = 1 << 30;
 
 // One segment of work: tiles [t_lo, t_hi) of unit (b, g) whose sequence has
 // L tokens; its result goes to split slot `slot` (or straight to o/lse when
-// `direct`); `first` segments also mark slots [nslots, S) unused.
+// `direct`).  Block-major schedule: `first` segments (slot 0) also mark
+// slots [nslots, S) unused.  Chunked schedule: the first segment of a chunk
+// marks [mark_lo, mark_hi) and [mark2_lo, mark2_hi) unused; `first` is
+// slot 0 (once per sequence and vector block).
 struct Seg {
   int b, g, L;
   int t_lo, t_hi;
-  int slot, nslots;
+  int slot, nslots;                              // block-major schedule
+  int mark_lo, mark_hi, mark2_lo, mark2_hi;      // chunked schedule
   bool first, direct, clamped;
 };
 
-// Persistent schedule, identical in every warp that walks it.
+// Persistent schedule, identical in every warp that walks it.  The list is
+// the tiles of all (sequence, vector block) units; a sequence with several
+// vector blocks is listed in chunks of CH tiles, all its blocks of a chunk
+// side by side, so that the CTAs holding the blocks of one chunk stream the
+// same KV tiles at about the same time and L2 serves the later readers.  A
+// chunk of one block spans at most SPC CTAs and owns SPC split slots.  CTA c
+// takes list tiles [lo, hi) = [c C, (c + 1) C).
 struct Sched {
-  const int* pre;  // [units + 1] first tile of each unit
+  const int* pre;  // [units + 1] first list tile of each unit (block-major)
   const int* len;  // [sequences] clamped length, | kClampedBit if clamped
-  int units, qblocks, C, lo, hi, c;
+  int units, qblocks, num_seqs, C, CH, SPC, S, lo, hi, c;
+  // Block-major schedule (one vector block per sequence): units in order.
   __device__ int first_unit() const {
     int a = 0, z = units;  // smallest u with pre[u + 1] > lo
     while (a < z) {
@@ -146,9 +157,51 @@ struct Sched {
     s.first = s.slot == 0;
     s.direct = false;
   }
+  // Chunked schedule: fills `s` with the segment that starts at list tile t
+  // (lo <= t < hi);
+  // returns the list tile where the next segment starts.
+  __device__ int seg_at(int t, Seg& s) const {
+    int a = 0, z = num_seqs - 1;  // the last sequence b with pre[b * qblocks] <= t
+    while (a < z) {
+      const int m = (a + z + 1) >> 1;
+      if (pre[m * qblocks] <= t) a = m; else z = m - 1;
+    }
+    const int b = a;
+    const int Ob = pre[b * qblocks];
+    const int Tb = pre[b * qblocks + 1] - Ob;  // tiles of the sequence
+    const int Jb = ceil_div(Tb, CH);
+    // list tiles of a full chunk (CH is 2^30 only with one block per sequence)
+    const int span = qblocks * CH;
+    const int x = t - Ob;
+    const int j = min(x / span, Jb - 1);
+    const int clen = j == Jb - 1 ? Tb - (Jb - 1) * CH : CH;  // tiles of chunk j
+    const int y = x - j * span;
+    const int g = y / clen;
+    const int in = y - g * clen;
+    const int vstart = Ob + j * span + g * clen;
+    const int vend = vstart + clen;
+    const int seg_end = min(hi, vend);
+    s.b = b;
+    s.g = g;
+    s.L = len[b] & ~kClampedBit;
+    s.clamped = (len[b] & kClampedBit) != 0;
+    s.t_lo = j * CH + in;
+    s.t_hi = s.t_lo + (seg_end - t);
+    const int cf = vstart / C;  // the CTA where chunk j of block g begins
+    s.slot = j * SPC + (c - cf);
+    const bool first = c == cf;
+    s.mark_lo = first ? j * SPC + ((vend - 1) / C - cf + 1) : 0;
+    s.mark_hi = first ? (j + 1) * SPC : 0;
+    s.mark2_lo = first && j == 0 ? Jb * SPC : 0;  // slots past the last chunk
+    s.mark2_hi = first && j == 0 ? S : 0;
+    s.first = s.slot == 0;
+    s.direct = false;
+    return seg_end;
+  }
 };
-
-template <int R, bool FP8, int MT, bool PERSIST>
+// PM: 0 = one CTA per (vector block, split); 1 = persistent, block-major
+// list (one vector block per sequence); 2 = persistent, chunked list.
+template <int R, bool FP8, int MT, int PM>
 __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
     decode_mma_kernel(const DecodeParams p,
                       const __grid_constant__ CUtensorMap tmap,
@@ -192,7 +245,7 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
   Sched sch;
   int nseg = 0;    // grid mode: 0 or 1 segment
   Seg gseg;        // grid mode segment
-  if constexpr (PERSIST) {
+  if constexpr (PM != 0) {
     const int units = p.num_seqs * qblocks;
     // pre[u + 1] = tiles of unit u, then an inclusive scan by warp 0
     for (int u = threadIdx.x; u < units; u += blockDim.x) {
@@ -232,7 +285,23 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
     sch.len = lens;
     sch.units = units;
     sch.qblocks = qblocks;
+    sch.num_seqs = p.num_seqs;
     sch.C = Cc;
+    sch.S = S;
+    sch.CH = 1 << 30;
+    sch.SPC = S;
+    if constexpr (PM == 2) {
+      // smallest m with (chunks) x (slots per chunk) <= S; m = ceil(max_n / C)
+      // (one chunk) always qualifies because C >= ceil(max_n / (S - 1))
+      for (int m = 1;; ++m) {
+        const int J = ceil_div(max_n, Cc * m);
+        if (J * (m + 1) <= S || J == 1) {
+          sch.CH = Cc * m;
+          sch.SPC = m + 1;
+          break;
+        }
+      }
+    }
     sch.c = blockIdx.x;
     sch.lo = blockIdx.x * Cc;
     sch.hi = min(total, sch.lo + Cc);
@@ -258,6 +327,7 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
     gseg.t_hi = start < end ? ceil_div(end, kBN) : gseg.t_lo;
     gseg.slot = split;
     gseg.nslots = S;
+    gseg.mark_lo = gseg.mark_hi = gseg.mark2_lo = gseg.mark2_hi = 0;
     gseg.first = false;
     gseg.direct = S == 1;
     gseg.clamped = false;  // counted above
@@ -299,12 +369,19 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
 
   // Walks the CTA's segments in order, calling f(seg, index).
   auto for_each_seg = [&](auto&& f) {
-    if constexpr (PERSIST) {
+    if constexpr (PM == 1) {
       int k = 0;
       for (int u = sch.first_unit(); u < sch.units && sch.pre[u] < sch.hi; ++u) {
         if (sch.pre[u + 1] <= max(sch.lo, sch.pre[u])) continue;  // empty unit
         Seg s;
         sch.seg(p, u, s);
+        if (!f(s, k++)) return;
+      }
+    } else if constexpr (PM == 2) {
+      int k = 0;
+      for (int t = sch.lo; t < sch.hi;) {
+        Seg s;
+        t = sch.seg_at(t, s);
         if (!f(s, k++)) return;
       }
     } else {
@@ -650,9 +727,16 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
         }
         if (q4 == 0 && tq == 0) {
           p.ws_lse[rec] = lse;
-          if (sg.first)  // slots this unit's partition leaves unused
+          // slots the partition leaves unused
+          if constexpr (PM == 2) {
+            for (int s = sg.mark_lo; s < sg.mark_hi; ++s)
+              p.ws_lse[(static_cast<int64_t>(row) * S + s) * H + h] = -INFINITY;
+            for (int s = sg.mark2_lo; s < sg.mark2_hi; ++s)
+              p.ws_lse[(static_cast<int64_t>(row) * S + s) * H + h] = -INFINITY;
+          } else if (sg.first) {
             for (int s = sg.nslots; s < S; ++s)
               p.ws_lse[(static_cast<int64_t>(row) * S + s) * H + h] = -INFINITY;
+          }
         }
       }
     }
@@ -664,13 +748,13 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
   });
 }
 
-template <int R, bool FP8, int MT, bool PERSIST>
+template <int R, bool FP8, int MT, int PM>
 cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmap, const QMaps& qmap,
                       int sm_count, cudaStream_t stream) {
   using C = MmaCfg<R, FP8, MT>;
   static bool attr_done = false;  // per instantiation; benign race
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<R, FP8, MT, PERSIST>,
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<R, FP8, MT, PM>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM);
     if (e != cudaSuccess) return e;
@@ -678,8 +762,8 @@ cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmap, const QMap
   }
   const int nvec = p.rows_per_seq * p.num_heads;
   const int qblocks = (nvec + 16 * MT - 1) / (16 * MT);
-  const dim3 grid = PERSIST ? dim3(sm_count) : dim3(qblocks, p.num_splits, p.num_seqs);
-  return launch_overlapped(decode_mma_kernel<R, FP8, MT, PERSIST>, grid, dim3(C::NTHREADS),
+  const dim3 grid = PM != 0 ? dim3(sm_count) : dim3(qblocks, p.num_splits, p.num_seqs);
+  return launch_overlapped(decode_mma_kernel<R, FP8, MT, PM>, grid, dim3(C::NTHREADS),
                            C::SMEM, stream, p, tmap, qmap);
 }
 
@@ -688,9 +772,13 @@ cudaError_t launch_r2(const DecodeParams& p, const CUtensorMap& tmap, const QMap
                       int sm_count, cudaStream_t stream) {
   const int qblocks = (p.rows_per_seq * p.num_heads + 16 * MT - 1) / (16 * MT);
   const int64_t units = static_cast<int64_t>(qblocks) * p.num_seqs;
-  if (p.num_splits > 1 && units <= kMaxPersistUnits)
-    return launch_mt<R, FP8, MT, true>(p, tmap, qmap, sm_count, stream);
-  return launch_mt<R, FP8, MT, false>(p, tmap, qmap, sm_count, stream);
+  if (p.num_splits > 1 && units <= kMaxPersistUnits) {
+    // (a single 16-vector block per CTA, MT = 1, means one block per sequence)
+    if constexpr (MT > 1)
+      if (qblocks > 1) return launch_mt<R, FP8, MT, 2>(p, tmap, qmap, sm_count, stream);
+    return launch_mt<R, FP8, MT, 1>(p, tmap, qmap, sm_count, stream);
+  }
+  return launch_mt<R, FP8, MT, 0>(p, tmap, qmap, sm_count, stream);
 }
 
 template <int R, bool FP8>

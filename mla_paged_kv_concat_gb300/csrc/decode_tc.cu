@@ -293,14 +293,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     const int Ob = pre[b * qblocks];
     const int Tb = pre[b * qblocks + 1] - Ob;  // tiles of the sequence
     const int Jb = cdiv(Tb, CH);
-    const int64_t span = static_cast<int64_t>(qblocks) * CH;  // list tiles of a full chunk
+    // list tiles of a full chunk (CH is 2^30 only with one block per sequence)
+    const int span = qblocks * CH;
     const int x = t - Ob;
-    const int j = static_cast<int>(min(static_cast<int64_t>(x) / span, static_cast<int64_t>(Jb - 1)));
+    const int j = min(x / span, Jb - 1);
     const int len = j == Jb - 1 ? Tb - (Jb - 1) * CH : CH;  // tiles of chunk j
-    const int y = x - static_cast<int>(j * span);
+    const int y = x - j * span;
     const int g = y / len;
     const int in = y - g * len;  // tile of the chunk where this segment starts
-    const int vstart = Ob + static_cast<int>(j * span) + g * len;
+    const int vstart = Ob + j * span + g * len;
     const int vend = vstart + len;
     const int seg_end = min(hi, vend);
     const int L = lens[b] & ~kClampedBit;
