@@ -268,3 +268,27 @@ def test_seq_len_beyond_table_is_clamped_and_counted(cuda_dev):
     assert int(d.err.item()) == 1
     o_ref, lse_ref = oracle_decode(w, oracle_cache(w))
     assert_close(o, lse, o_ref, lse_ref, what="clamp")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_split_count_at_its_cap(cuda_dev, path):
+    """The split rule's cap, 2 x SMs, reached by a 160k-token sequence next to
+    short ones (most of the 304 slots of the short rows stay unused); every
+    (row, head) compared."""
+    H = 16 if path == mla.MLA_PATH_MMA_SYNC else 128
+    w = W.make_workload("cap", seed=77, seq_lens=[160_000, 3, 700], num_heads=H,
+                        pool_blocks=2600)
+    S = mla.mla_num_kv_splits(w.max_seq_len, sm_count())
+    assert S == 2 * sm_count()
+    pairs = None if H == 16 else sample_pairs(w, 48, seed=8)
+    d, o, lse = _run(w, S, path, pairs=pairs)
+    assert int(d.err.item()) == 0
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_many_splits_on_short_sequences(cuda_dev, path):
+    """More split slots than tiles: every row's unused slots are marked and
+    skipped by the merge."""
+    H = 16 if path == mla.MLA_PATH_MMA_SYNC else 128
+    w = W.make_workload("shortS", seed=78, seq_lens=[1, 64, 65, 200, 0], num_heads=H)
+    _run(w, 2 * sm_count(), path)
