@@ -2,8 +2,12 @@
  * mla.h - C ABI of libmla: MLA decode over a paged latent KV cache on GB300
  * (sm_103a).
  *
- * The library implements three steps of multi-head latent attention (MLA)
- * decode as described on the vLLM pages it restates:
+ * The library implements the decode hot path of multi-head latent attention
+ * (MLA) as described on the vLLM pages it restates -- the cache write of a
+ * step's new tokens (plain, or fused with the RMSNorm of the latent and the
+ * rotary embedding), the split-KV attention pass over the paged latent cache
+ * and the log-sum-exp merge -- plus the cross-shard merge of decode context
+ * parallelism and prepared, CUDA-graph-safe plans of a whole step:
  *
  *   [diff] "frozenleaves/vllm compare v0.11.0...mla_cuda_graphs" ("fix TP"),
  *          a unified diff of vLLM, cited by file section;
@@ -60,8 +64,10 @@ typedef enum {
  * MLA_ERR_UNSUPPORTED. */
 typedef enum {
   MLA_PATH_AUTO = 0,
-  MLA_PATH_MMA_SYNC = 1, /* warp-level bf16 MMA, any head count            */
-  MLA_PATH_TCGEN05 = 2   /* tcgen05/TMEM kernel for >= 64 heads, bf16 cache */
+  MLA_PATH_MMA_SYNC = 1, /* warp-level bf16 MMA: every cache type and shape   */
+  MLA_PATH_TCGEN05 = 2   /* tcgen05/TMEM, 2-CTA clusters of 128 query vectors:
+                            bf16 cache with kv_lora_rank 512; AUTO takes it
+                            from 128 query vectors (rows x heads) per sequence */
 } mla_decode_path;
 
 /*
