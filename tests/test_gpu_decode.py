@@ -135,6 +135,35 @@ def test_small_shapes(cuda_dev, case, splits, path):
     _run(w, splits, path)
 
 
+@pytest.mark.parametrize("splits", [1, 8])
+@pytest.mark.parametrize("q_exp,R,H,rows", [(20, 256, 32, 1), (-30, 512, 16, 1),
+                                            (-100, 256, 16, 2), (None, 512, 32, 1),
+                                            (None, 256, 128, 1)])
+def test_fp8_query_magnitudes(cuda_dev, q_exp, R, H, rows, splits):
+    """An fp8 cache against queries of extreme magnitude: every element times
+    2^q_exp (far outside the fp8 and f16 ranges) with sm_scale times 2^-q_exp
+    so that the scores stay moderate, or heads of different magnitudes
+    (None: head h times 2^(h mod 5 - 2)).  The query keeps its bf16 range
+    through the kernel, so every case matches the oracle."""
+    w = W.make_workload(f"fp8q{q_exp}", seed=410 + (q_exp or 0) % 97 + H, pool_blocks=None,
+                        seq_lens=[150, 33, 700][: 3 - rows + 1], num_heads=H,
+                        rows_per_seq=rows, kv_lora_rank=R, kv_fp8=True, kv_scale=0.05,
+                        write="all")
+    q = w.q.double()
+    if q_exp is None:
+        q = q * (2.0 ** (torch.arange(H, dtype=torch.float64) % 5 - 2))[None, :, None]
+        sm = w.sm_scale
+    else:
+        q = q * 2.0 ** q_exp
+        sm = float(np.float32(w.sm_scale) * np.float32(2.0 ** -q_exp))
+    q32 = q.float()
+    assert torch.isfinite(q32).all()
+    w.q = q32.bfloat16()
+    assert torch.equal(w.q.double(), q)  # power-of-two scaling is exact in bf16
+    w.sm_scale = sm
+    _run(w, splits, mla.MLA_PATH_MMA_SYNC)
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_forced_kernel_rejects_what_it_does_not_cover(cuda_dev, path):
     w = W.make_workload("rej", seed=64, seq_lens=[100], num_heads=16, kv_lora_rank=256)
