@@ -41,7 +41,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 3)
   if (gw >= p.num_rows * H) return;
   const int row = gw / H, h = gw % H;
   const int S = p.num_splits;
+  const int64_t rec0 = static_cast<int64_t>(row) * S * H + h;  // split 0
+  // The sequence length and the lse of the first 32 slots are loaded
+  // together (one round trip); the slots of an empty sequence hold stale
+  // values that are never used.
   int L = __ldg(p.seq_lens + row / p.rows_per_seq);
+  const float ls0 = lane < S ? p.ws_lse[rec0 + static_cast<int64_t>(lane) * H] : -INFINITY;
   const int Lmax = p.max_blocks * p.block_size;
   L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
   uint16_t* orow = p.o + static_cast<int64_t>(gw) * R;
@@ -52,9 +57,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 3)
     if (lane == 0) p.lse[gw] = -INFINITY;
     return;
   }
-  const int64_t rec0 = static_cast<int64_t>(row) * S * H + h;  // split 0
-  float M = -INFINITY;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, p.ws_lse[rec0 + static_cast<int64_t>(s) * H]);
+  float M = ls0;
+  for (int s = lane + 32; s < S; s += 32) M = fmaxf(M, p.ws_lse[rec0 + static_cast<int64_t>(s) * H]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
@@ -67,7 +71,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 3)
     // kInFlight non-empty slots are loaded together, then added in slot
     // order (few rows per warp, many warps per SM).
     const int s = c + lane;
-    const float ls = s < S ? p.ws_lse[rec0 + static_cast<int64_t>(s) * H] : -INFINITY;
+    const float ls =
+        c == 0 ? ls0 : (s < S ? p.ws_lse[rec0 + static_cast<int64_t>(s) * H] : -INFINITY);
     const float w = ls == -INFINITY ? 0.f : __expf(ls - M);
     den += w;
     uint32_t mask = __ballot_sync(0xffffffffu, w != 0.f);
