@@ -39,6 +39,49 @@ def test_every_declared_symbol_is_exported(lib):
         assert name in _lib.SIGNATURES, name
 
 
+def _c_to_ctypes(ctype: str):
+    """The ctypes class a C parameter or return type of mla.h marshals as."""
+    t = ctype.replace("const", "").strip()
+    if t == "void":
+        return None
+    if "*" in t:
+        return "pointer"
+    return {"int64_t": ctypes.c_int64, "int": ctypes.c_int, "float": ctypes.c_float,
+            "size_t": ctypes.c_size_t, "mla_status": ctypes.c_int, "mla_kv_dtype": ctypes.c_int,
+            "mla_decode_path": ctypes.c_int}[t]
+
+
+def _is_pointer(ct) -> bool:
+    return ct in (ctypes.c_void_p, ctypes.c_char_p) or (
+        isinstance(ct, type) and issubclass(ct, ctypes._Pointer))
+
+
+def test_binding_signatures_match_the_header_prototypes():
+    """Every prototype's return type, parameter count and parameter types
+    agree with the ctypes table the binding loads the library with, so a
+    parameter added to or moved in the header cannot go unnoticed."""
+    text = open(os.path.join(ROOT, "include", "mla.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    protos = re.findall(r"([A-Za-z_][\w\s\*]*?)\b(mla_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text)
+    assert {name for _, name, _ in protos} == set(_lib.SIGNATURES)
+    for ret, name, params in protos:
+        restype, argtypes = _lib.SIGNATURES[name]
+        want = _c_to_ctypes(ret)
+        if want == "pointer":
+            assert restype is ctypes.c_char_p, name
+        else:
+            assert restype is want, name
+        plist = [] if params.strip() == "void" else [x.strip() for x in params.split(",")]
+        assert len(plist) == len(argtypes), (name, len(plist), len(argtypes))
+        for i, (decl, got) in enumerate(zip(plist, argtypes)):
+            ctype = re.sub(r"\b\w+\s*$", "", decl).strip()  # drop the parameter name
+            want = _c_to_ctypes(ctype)
+            if want == "pointer":
+                assert _is_pointer(got), (name, i, decl)
+            else:
+                assert got is want, (name, i, decl, got)
+
+
 def test_split_rule_and_workspace_size(lib):
     assert mla.mla_num_kv_splits(4096, 152) == 8
     assert mla.mla_num_kv_splits(0, 152) == 1
