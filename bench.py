@@ -146,17 +146,63 @@ def job_throughput(bytes_per_step: int, steps: int, world: int, total_ms: float)
 
 
 # ---------------------------------------------------------------- our arm
-def run_ours(args, rank, world, local_rank):
+# Steps of each record in the ``configs`` list (the headline workload takes
+# --steps).
+CONFIG_STEPS = 10
+# The other workloads, measured after the headline one and reported under
+# ``configs``: (workload, num_kv_splits = 1).
+OTHER_CONFIGS = (("per_shard", False), ("full_head", False), ("full_head", True),
+                 ("fp8_small", False), ("tiny", False))
+
+
+def _roofline(w, args, workload, deterministic, kv_bytes, flops, s1_ms):
+    """Roofline record of the stage-1 kernel: the KV bytes (or, above the
+    ridge, the flops) of one launch over its CUDA-event duration, against the
+    measured peak."""
+    hbm, bf16, src = _peaks()
+    R, H = w.kv_lora_rank, w.num_heads
+    achieved = kv_bytes / (s1_ms * 1e-3) / 1e9
+    # the stage-1 kernel the library picks (tcgen05 for bf16, R = 512 and at
+    # least 128 query vectors per sequence; warp MMA otherwise)
+    tc = (not w.kv_fp8) and R == 512 and w.rows_per_seq * H >= 128 and args.path != 1
+    tc = tc or args.path == 2
+    kernel_src = "decode_tc.cu" if tc else "decode_mma.cu"
+    traffic = _traffic_record(os.path.join(ROOT, "mla_paged_kv_concat_gb300", "csrc",
+                                           kernel_src),
+                              workload + ("_s1" if deterministic else ""))
+    kname = ("decode_tc_kernel" if tc else "decode_mma_kernel") + " (stage 1)"
+    if flops / (bf16 * 1e12) > kv_bytes / (hbm * 1e9):
+        # above the ridge (several query rows share each cached row): the
+        # contraction's flops against the bf16 tensor peak
+        tf = flops / (s1_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "kernel": kname, "achieved": round(tf, 1),
+                "peak": bf16, "unit": "TFLOP/s", "frac": round(tf / bf16, 4),
+                "traffic": traffic,
+                "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops, burst)",
+                "hbm_gbs": round(achieved, 1)}
+    return {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
+            "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+            "traffic": traffic,
+            "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs, burst)"}
+
+
+def run_ours(args, rank, world, local_rank, workload=None, deterministic=None, light=False):
+    """One workload's measurement.  light: the per-config record of the
+    ``configs`` list (no e2e pass), with its own step count."""
     import torch
     import mla_paged_kv_concat_gb300 as mla
     from mla_paged_kv_concat_gb300 import workloads as W
 
+    workload = args.workload if workload is None else workload
+    deterministic = args.deterministic if deterministic is None else deterministic
+    steps = min(args.steps, CONFIG_STEPS) if light else args.steps
+    warmup = 3 if light else args.warmup
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     lib = mla.load()
-    w = W.make(args.workload)
+    w = W.make(workload)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    S = 1 if args.deterministic else mla.mla_num_kv_splits(w.max_seq_len, sms)
+    S = 1 if deterministic else mla.mla_num_kv_splits(w.max_seq_len, sms)
     R, P, D, H = w.kv_lora_rank, w.rope_dim, w.head_dim, w.num_heads
     rows, seqs = w.num_rows, w.num_seqs
     kvd = mla.MLA_KV_FP8_E4M3 if w.kv_fp8 else mla.MLA_KV_BF16
@@ -287,7 +333,7 @@ def run_ours(args, rank, world, local_rank):
         if dist is not None:
             dist.barrier()
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush_l2()
         step_events()
         flush_l2()
@@ -298,12 +344,12 @@ def run_ours(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clk:
         barrier()
         torch.cuda.synchronize(dev)
-        for _ in range(args.steps):
+        for _ in range(steps):
             flush_l2()
             evs.append(step_events())
         torch.cuda.synchronize(dev)
         barrier()
-        for _ in range(args.steps):
+        for _ in range(steps):
             flush_l2()
             kevs.append(step_kernel_events())
         torch.cuda.synchronize(dev)
@@ -312,11 +358,31 @@ def run_ours(args, rank, world, local_rank):
     t_merge = [e[2].elapsed_time(e[3]) for e in kevs]
     t_step = [e[0].elapsed_time(e[1]) for e in evs]
     total_ms = max_over_ranks(float(np.sum(t_step)), dev)
-    ms_step = total_ms / args.steps
+    ms_step = total_ms / steps
     kv_bytes = w.kv_bytes()
     flops = w.flops()
-    n_units = world * args.steps
-    value = job_throughput(kv_bytes, args.steps, world, total_ms)
+    n_units = world * steps
+    value = job_throughput(kv_bytes, steps, world, total_ms)
+    hbm, bf16, src = _peaks()
+    s1_ms = float(np.mean(t_s1))
+    roofline = _roofline(w, args, workload, deterministic, kv_bytes, flops, s1_ms)
+    roof_t = max(kv_bytes / (hbm * 1e9), flops / (bf16 * 1e12))
+    kernel_ms = {("norm_rope_cache_write" if args.fused_write else "cache_write"):
+                 round(float(np.mean(t_write)), 5),
+                 "decode_splitkv": round(s1_ms, 5),
+                 "decode_merge": round(float(np.mean(t_merge)), 5)}
+    if light:
+        if rank != 0:
+            return None
+        return {"workload": workload + ("_s1" if deterministic else ""), "num_kv_splits": S,
+                "rows": rows, "heads": H, "kv_tokens": int(w.seq_lens.sum()),
+                "kv_bytes": kv_bytes, "steps": steps, "warmup": warmup,
+                "ms_per_step": round(ms_step, 5), "value": round(value, 2), "unit": "GB/s",
+                "tflops": round(flops * n_units / (total_ms * 1e-3) / 1e12, 2),
+                "kernel_ms": kernel_ms, "roofline": roofline,
+                "step_roofline_frac": round(roof_t / (ms_step * 1e-3), 4),
+                "decode_rows_per_s": round(rows / ((s1_ms + float(np.mean(t_merge))) * 1e-3), 1),
+                "gpu_launches": launches_per_step * steps, "clocks": clk.summary()}
 
     # ---- e2e through the C ABI with host buffers (pinned), copies timed.
     # The step's inputs sit in one pinned host block and go over in one
@@ -372,12 +438,12 @@ def run_ours(args, rank, world, local_rank):
             assert st == 0, st
         h_outb.copy_(d_outb, non_blocking=True)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush_l2()
         e2e_step()
     torch.cuda.synchronize(dev)
     e2e_ms = []
-    for _ in range(args.steps):
+    for _ in range(steps):
         flush_l2()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -386,7 +452,7 @@ def run_ours(args, rank, world, local_rank):
         e2e_ms.append((a, b))
     torch.cuda.synchronize(dev)
     e2e_serial_total = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in e2e_ms)), dev)
-    e2e_serial_value = job_throughput(kv_bytes, args.steps, world, e2e_serial_total)
+    e2e_serial_value = job_throughput(kv_bytes, steps, world, e2e_serial_total)
 
     # ---- e2e as a serving loop runs it: step i's inputs go up on one copy
     # stream while step i - 1 computes, results come back on another; two
@@ -424,57 +490,31 @@ def run_ours(args, rank, world, local_rank):
                     ev["out", i].record(down)
             stream.wait_event(ev["out", k - 1])
 
-        pipelined(max(args.warmup, 2))
+        pipelined(max(warmup, 2))
         torch.cuda.synchronize(dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         up.wait_stream(stream)
-        pipelined(args.steps)
+        pipelined(steps)
         b.record(stream)
         torch.cuda.synchronize(dev)
         e2e_pipe_total = max_over_ranks(a.elapsed_time(b), dev)
     l2_bytes = 129e6
     use_pipe = e2e_pipe_total is not None and kv_bytes > l2_bytes
     e2e_total = e2e_pipe_total if use_pipe else e2e_serial_total
-    e2e_value = job_throughput(kv_bytes, args.steps, world, e2e_total)
+    e2e_value = job_throughput(kv_bytes, steps, world, e2e_total)
     if int(err.item()) != 0:
         print(f"warning: device error counter {int(err.item())}", file=sys.stderr)
 
     if rank != 0:
         return None
-    hbm, bf16, src = _peaks()
-    s1_ms = float(np.mean(t_s1))
-    achieved = kv_bytes / (s1_ms * 1e-3) / 1e9
-    # the stage-1 kernel the library picks (tcgen05 for bf16, R = 512 and at
-    # least 128 query vectors per sequence; warp MMA otherwise)
-    tc = (not w.kv_fp8) and R == 512 and w.rows_per_seq * H >= 128 and args.path != 1
-    tc = tc or args.path == 2
-    kernel_src = "decode_tc.cu" if tc else "decode_mma.cu"
-    traffic = _traffic_record(os.path.join(ROOT, "mla_paged_kv_concat_gb300", "csrc",
-                                           kernel_src), args.workload)
-    roof_t = max(kv_bytes / (hbm * 1e9), flops / (bf16 * 1e12))
-    kname = ("decode_tc_kernel" if tc else "decode_mma_kernel") + " (stage 1)"
-    if flops / (bf16 * 1e12) > kv_bytes / (hbm * 1e9):
-        # above the ridge (several query rows share each cached row): the
-        # contraction's flops against the bf16 tensor peak
-        tf = flops / (s1_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": kname, "achieved": round(tf, 1),
-                    "peak": bf16, "unit": "TFLOP/s", "frac": round(tf / bf16, 4),
-                    "traffic": traffic,
-                    "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops, burst)",
-                    "hbm_gbs": round(achieved, 1)}
-    else:
-        roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
-                    "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                    "traffic": traffic,
-                    "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs, burst)"}
     line = {
         "metric": "MLA decode KV GB/s & TFLOPS as % of roofline; decode rows/s at 1 GB300",
         "value": round(value, 2),
         "unit": "GB/s",
         "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
+        "steps": steps,
+        "warmup": warmup,
         "ms_per_step": round(ms_step, 5),
         "higher_is_better": True,
         "scaling": "weak",
@@ -482,7 +522,8 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "bf16" if not w.kv_fp8 else "bf16 q / e4m3 cache",
         "data": "synthetic (seeded N(0,1) bf16; NaN-poisoned unused cache memory)",
         "config": {
-            "workload": args.workload, "num_seqs": seqs, "rows": rows, "heads": H,
+            "workload": workload + ("_s1" if deterministic else ""), "num_seqs": seqs,
+            "rows": rows, "heads": H,
             "kv_lora_rank": R, "rope_dim": P, "block_size": bs,
             "seq_lens": [int(w.seq_lens.min()), int(w.seq_lens.max())],
             "kv_tokens": int(w.seq_lens.sum()), "new_tokens": T, "num_kv_splits": S,
@@ -502,21 +543,18 @@ def run_ours(args, rank, world, local_rank):
         "cache_write_gbs": round(T * D * (2 + (1 if w.kv_fp8 else 2))
                                  / (float(np.mean(t_write)) * 1e-3) / 1e9, 1),
         "step_roofline_frac": round(roof_t / (ms_step * 1e-3), 4),
-        "kernel_ms": {("norm_rope_cache_write" if args.fused_write else "cache_write"):
-                      round(float(np.mean(t_write)), 5),
-                      "decode_splitkv": round(s1_ms, 5),
-                      "decode_merge": round(float(np.mean(t_merge)), 5)},
+        "kernel_ms": kernel_ms,
         "roofline": roofline,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_total / args.steps, 5),
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_total / steps, 5),
                 "mode": ("pipelined: copies of step i+1 overlap step i, no L2 flush "
                          "(a step's KV bytes exceed L2)") if use_pipe else
                         "serial: copy in, step, copy out; L2 flushed between steps",
                 "serial_value": round(e2e_serial_value, 2),
-                "serial_ms_per_step": round(e2e_serial_total / args.steps, 5),
-                "pipelined_ms_per_step": round(e2e_pipe_total / args.steps, 5)
+                "serial_ms_per_step": round(e2e_serial_total / steps, 5),
+                "pipelined_ms_per_step": round(e2e_pipe_total / steps, 5)
                 if e2e_pipe_total is not None else None},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step * steps,
         "clocks": clk.summary(),
     }
     return line
@@ -585,15 +623,24 @@ def run_lse_merge(args):
 
 
 # ---------------------------------------------------------------- oracle timing
-def oracle_sample(workload: str, n_rows: int):
-    """Time the oracle (as it stands) on the first n_rows rows of the workload:
-    the cache write of those rows' new tokens and the decode of those rows."""
+# Oracle rows per sample: the cpu_baseline of our arm (about 5-20 s of fp64
+# work on 16 cores) and each step of the reference arm (a few seconds at most).
+CPU_ROWS = {"tiny": 2, "per_shard": 16, "full_head": 4, "fp8_small": 8, "long_multirow": 2}
+REF_ROWS = {"tiny": 2, "per_shard": 4, "full_head": 1, "fp8_small": 4, "long_multirow": 1}
+
+
+def oracle_sample(w, n_rows: int):
+    """Time the oracle (as it stands) on the first n_rows rows of workload w:
+    the cache write of the batch's new tokens and the decode of those rows.
+    Fewer rows than a sequence holds sample that many of its first sequence's
+    rows (each row attends to the whole sequence on its own)."""
     import oracle
-    from mla_paged_kv_concat_gb300 import workloads as W
-    w = W.make(workload)
-    n_rows = min(n_rows, w.num_rows)
-    n_seqs = (n_rows + w.rows_per_seq - 1) // w.rows_per_seq
-    n_rows = n_seqs * w.rows_per_seq
+    n_rows = max(1, min(n_rows, w.num_rows))
+    if n_rows <= w.rows_per_seq:
+        n_seqs = 1
+    else:
+        n_seqs = (n_rows + w.rows_per_seq - 1) // w.rows_per_seq
+        n_rows = n_seqs * w.rows_per_seq
     cache = w.kv_cache.copy()
     t0 = time.perf_counter()
     oracle.cache_write(w.kv_c, w.k_pe, w.slot_mapping, cache, block_size=w.block_size,
@@ -604,11 +651,14 @@ def oracle_sample(workload: str, n_rows: int):
                   sm_scale=w.sm_scale, kv_is_fp8=w.kv_fp8, kv_scale=w.kv_scale)
     dt = time.perf_counter() - t0
     kv = int(w.seq_lens[:n_seqs].astype(np.int64).sum()) * w.head_dim * w.kv_elem_bytes()
-    return kv / dt / 1e9, dt, n_rows, oracle.max_threads(), w
+    return kv / dt / 1e9, dt, n_rows, oracle.max_threads()
 
 
-def cpu_baseline(workload: str, n_rows: int):
-    gbs, dt, n, cores, w = oracle_sample(workload, n_rows)
+def cpu_baseline(workload: str, n_rows):
+    from mla_paged_kv_concat_gb300 import workloads as W
+    w = W.make(workload)
+    n_rows = CPU_ROWS.get(workload, 4) if n_rows is None else n_rows
+    gbs, dt, n, cores = oracle_sample(w, n_rows)
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{workload}: cache write of all {w.slot_mapping.size} new tokens + "
                       f"fp64 decode of rows 0..{n - 1} (all {w.num_heads} heads), "
@@ -618,9 +668,12 @@ def cpu_baseline(workload: str, n_rows: int):
 def run_reference(args, rank, world):
     if rank != 0:
         return None
+    from mla_paged_kv_concat_gb300 import workloads as W
+    w = W.make(args.workload)
+    n_rows = REF_ROWS.get(args.workload, 4) if args.ref_rows is None else args.ref_rows
     vals, dts = [], []
     for i in range(args.warmup + args.steps):
-        gbs, dt, n, cores, w = oracle_sample(args.workload, args.ref_rows)
+        gbs, dt, n, cores = oracle_sample(w, n_rows)
         if i >= args.warmup:
             vals.append(gbs)
             dts.append(dt)
@@ -641,18 +694,35 @@ def run_reference(args, rank, world):
     }
 
 
+def relaunch_under_torchrun(n: int) -> None:
+    """`--gpus N` without a launcher: start N ranks of this same command under
+    torch.distributed.run (one node, rendezvous on 127.0.0.1) and exit with
+    their status."""
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr=127.0.0.1", f"--master-port={port}",
+           os.path.abspath(__file__)] + sys.argv[1:]
+    sys.exit(subprocess.call(cmd))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="per_shard")
+    ap.add_argument("--workload", default="long_multirow",
+                    help="the headline workload (default: the largest one-GPU batch)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="measure the headline workload only (no configs list)")
     ap.add_argument("--deterministic", action="store_true", help="num_kv_splits = 1")
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 mma.sync, 2 tcgen05")
-    ap.add_argument("--cpu-rows", type=int, default=16,
+    ap.add_argument("--cpu-rows", type=int, default=None,
                     help="rows of the workload in the oracle's cpu_baseline sample")
-    ap.add_argument("--ref-rows", type=int, default=4,
+    ap.add_argument("--ref-rows", type=int, default=None,
                     help="rows per step in the --impl reference sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--api", choices=["plan", "calls"], default="plan",
@@ -668,6 +738,8 @@ def main():
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        relaunch_under_torchrun(args.gpus)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
@@ -686,6 +758,19 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     line = run_ours(args, rank, world, local_rank)
+    if not args.no_configs:
+        # every other workload, one record each (replicas: each rank runs its
+        # own; rank 0 reports)
+        import torch
+        records = []
+        for wl, det in OTHER_CONFIGS:
+            if wl == args.workload and det == args.deterministic:
+                continue
+            torch.cuda.empty_cache()
+            records.append(run_ours(args, rank, world, local_rank, workload=wl,
+                                    deterministic=det, light=True))
+        if line is not None:
+            line["configs"] = records
     if line is not None:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_rows)

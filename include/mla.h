@@ -181,7 +181,9 @@ int mla_num_kv_splits(int64_t max_seq_len, int sm_count);
  * num_kv_splits == 1 (the single pass writes o and lse directly).  Same size
  * as the pages' attn_logits [B, H, S, R+1] fp32 buffer ([note] Data flow;
  * [api] _reserve_attn_logits_workspace), laid out as o partials
- * [rows][S][H][R] followed by lse partials [rows][S][H].
+ * [rows][S][H][R] followed by lse partials [rows][S][H].  Returns SIZE_MAX
+ * when the product does not fit a size_t; every decode entry point then
+ * refuses the call with MLA_ERR_WORKSPACE_TOO_SMALL.
  */
 size_t mla_decode_workspace_bytes(int num_rows, int num_heads,
                                   int num_kv_splits, int kv_lora_rank);
@@ -326,6 +328,8 @@ mla_status mla_decode_merge(int num_rows, int num_heads, int kv_lora_rank,
  *
  * The first call on a device (with that device current) looks up the
  * array's device address; make that first call before any stream capture.
+ * The address is kept with the context's id: after cudaDeviceReset the next
+ * call looks it up again (again, before any capture).
  * All calls share the one array: calls whose kernels overlap on the GPU
  * (other streams, other host threads on the same device) race on it and
  * must be serialised by the caller.

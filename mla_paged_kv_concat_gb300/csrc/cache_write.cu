@@ -79,9 +79,13 @@ __device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
 // division is done.  Quotients too small for the relative bound (|q| below
 // 2^-104) are all +-0 in both formats, with the sign that both sides agree
 // on; |q| is clamped to 2^100 (every such value saturates to the largest
-// finite code either way); NaN quotients take the division.
+// finite code either way); NaN quotients take the division.  The bound needs
+// r to be a normal number: for a scale below 2^-126 (r infinite) or at or
+// above 2^126 (r subnormal, with a larger relative error) the caller passes
+// r = 0 and every element takes the division.
 template <int FMT>
 __device__ __forceinline__ uint32_t quant2(float x0, float x1, float s, float r) {
+  if (r == 0.f) return fp8x2<FMT>(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
   float q0 = x0 * r, q1 = x1 * r;
   if (q0 != q0 || q1 != q1) return fp8x2<FMT>(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
   q0 = fminf(fmaxf(q0, -0x1p100f), 0x1p100f);
@@ -154,7 +158,10 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NR ? 3 : 1)
   const int lane = threadIdx.x & 31;
   const int D = a.R + a.P;
   const float s = FP8 ? __ldg(a.scale) : 1.0f;
-  const float r = FP8 ? __fdiv_rn(1.0f, s) : 1.0f;  // RN(1/s), as quant2's bound assumes
+  // RN(1/s), as quant2's bound assumes; 0 (always divide) unless it is a
+  // normal number
+  const float r_div = FP8 ? __fdiv_rn(1.0f, s) : 1.0f;
+  const float r = fabsf(r_div) >= 0x1p-126f && fabsf(r_div) <= 0x1p126f ? r_div : 0.f;
   // Warp-stride loop over groups of kTokensPerWarp consecutive tokens (the
   // grid is sized to the GPU, not to the token count).  All loads of a group
   // (rows and slots) are issued before any of them is used, so that each
@@ -305,27 +312,32 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NR ? 3 : 1)
 }
 
 // Launches the fused variant KERNEL on min(need, one wave) CTAs, the wave
-// being the CTAs resident at once (per SM x SMs of the current device,
-// queried once): with its one-row warps and three CTAs per SM, a grid past
-// one wave left a partial last wave (whole-cache fp8 fused write 259 against
-// 247 us).  The plain write keeps its larger grid, which measured faster
-// than one wave (148 against 156 us).
+// being the CTAs resident at once (per SM x SMs of the current device, both
+// queried once per device): with its one-row warps and three CTAs per SM, a
+// grid past one wave left a partial last wave (whole-cache fp8 fused write
+// 259 against 247 us).  The plain write keeps its larger grid, which
+// measured faster than one wave (148 against 156 us).  A failed query is
+// returned as the launch's error (nothing is launched).
 template <auto KERNEL>
-void launch_one_wave(int64_t need, const CacheWriteArgs& a, cudaStream_t stream) {
-  static const int64_t wave = [] {
-    int dev = 0, sms = 148, per_sm = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, KERNEL, kWarpsPerCta * 32, 0) !=
-            cudaSuccess ||
-        per_sm < 1) {
-      (void)cudaGetLastError();  // a failed query is not the launch's error
-      per_sm = 1;
-    }
-    return static_cast<int64_t>(per_sm) * sms;
-  }();
+cudaError_t launch_one_wave(int64_t need, const CacheWriteArgs& a, cudaStream_t stream) {
+  static std::atomic<int> per_sm_cache[kMaxDevices] = {};
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  e = device_sm_count(&sms);
+  if (e != cudaSuccess) return e;
+  int per_sm = per_sm_cache[dev].load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, KERNEL, kWarpsPerCta * 32, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    per_sm_cache[dev].store(per_sm, std::memory_order_relaxed);
+  }
+  const int64_t wave = static_cast<int64_t>(per_sm) * sms;
   const dim3 grid(static_cast<unsigned>(need < wave ? need : wave));
   KERNEL<<<grid, dim3(kWarpsPerCta * 32), 0, stream>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -372,9 +384,9 @@ cudaError_t launch_cache_write(const void* kv_c, int64_t kv_c_stride,
                    ((block_stride * elt) % 16 == 0) &&
                    ((static_cast<size_t>(R + P) * elt) % 16 == 0) &&
                    ((static_cast<size_t>(R) * elt) % (fp8 ? 8 : 16) == 0);
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0;
+  cudaError_t e = device_sm_count(&sms);
+  if (e != cudaSuccess) return e;
   const int64_t per_cta = static_cast<int64_t>(kWarpsPerCta) * kTokensPerWarp;
   const int64_t need = (static_cast<int64_t>(num_tokens) + per_cta - 1) / per_cta;
   const dim3 grid(static_cast<unsigned>(need < 8 * sms ? need : 8 * sms));
@@ -433,13 +445,9 @@ cudaError_t launch_norm_rope_cache_write(const void* kv_c, int64_t kv_c_stride, 
   a.q_pe_head_stride = q_pe_head_stride;
   a.q_heads = q_heads;
   const int64_t need = (static_cast<int64_t>(num_tokens) + kWarpsPerCta - 1) / kWarpsPerCta;
-  if (fmt == kE4M3)
-    launch_one_wave<cache_write_kernel<kE4M3, true, true>>(need, a, stream);
-  else if (fmt == kE5M2)
-    launch_one_wave<cache_write_kernel<kE5M2, true, true>>(need, a, stream);
-  else
-    launch_one_wave<cache_write_kernel<kBf16, true, true>>(need, a, stream);
-  return cudaGetLastError();
+  if (fmt == kE4M3) return launch_one_wave<cache_write_kernel<kE4M3, true, true>>(need, a, stream);
+  if (fmt == kE5M2) return launch_one_wave<cache_write_kernel<kE5M2, true, true>>(need, a, stream);
+  return launch_one_wave<cache_write_kernel<kBf16, true, true>>(need, a, stream);
 }
 
 }  // namespace mla

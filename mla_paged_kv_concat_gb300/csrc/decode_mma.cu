@@ -752,14 +752,9 @@ template <int R, bool FP8, int MT, int PM>
 cudaError_t launch_mt(const DecodeParams& p, const CUtensorMap& tmap, const QMaps& qmap,
                       int sm_count, cudaStream_t stream) {
   using C = MmaCfg<R, FP8, MT>;
-  static bool attr_done = false;  // per instantiation; benign race
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<R, FP8, MT, PM>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};  // per instantiation, one bit per device
+  cudaError_t e = set_smem_attr_once(decode_mma_kernel<R, FP8, MT, PM>, C::SMEM, attr_done);
+  if (e != cudaSuccess) return e;
   const int nvec = p.rows_per_seq * p.num_heads;
   const int qblocks = (nvec + 16 * MT - 1) / (16 * MT);
   const dim3 grid = PM != 0 ? dim3(sm_count) : dim3(qblocks, p.num_splits, p.num_seqs);

@@ -954,13 +954,9 @@ int tc_split_group(const DecodeParams& p, int sm_count) {
 
 cudaError_t launch_decode_tc(const DecodeParams& p, const CUtensorMap& tmap,
                              int split_group, int sm_count, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(
-        decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};  // one bit per device
+  cudaError_t e = set_smem_attr_once(decode_tc_kernel, TC_SMEM, attr_done);
+  if (e != cudaSuccess) return e;
   const int qblocks = (p.rows_per_seq * p.num_heads + 127) / 128;
   const int64_t units = static_cast<int64_t>(qblocks) * p.num_seqs;
   if (p.num_splits > 1 && units <= kMaxPersistUnits) {

@@ -5,11 +5,40 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace mla {
 
 // Largest number of (sequence, 16-vector block) units the persistent
 // warp-MMA schedule handles; larger batches use one CTA per (unit, split).
 constexpr int kMaxPersistUnits = 512;
+
+// Device ordinals the per-device caches below cover.
+constexpr int kMaxDevices = 64;
+
+// SM count of the current device, queried once per device and cached (calls
+// from several host threads may race to fill an entry; they store the same
+// value).  Returns the query's error instead of guessing a count.
+cudaError_t device_sm_count(int* sms);
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device: the attribute belongs to the device, so a process
+// that drives several GPUs sets it on each.  `done` is one bit per device
+// ordinal, owned by the caller (one per kernel instantiation).  Threads that
+// race here set the same value; the bit is published only after success.
+template <typename K>
+inline cudaError_t set_smem_attr_once(K kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const uint64_t bit = uint64_t{1} << dev;
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  done.fetch_or(bit, std::memory_order_release);
+  return cudaSuccess;
+}
 
 // Arguments of one decode call after host validation.  Pointers are device
 // memory.  rows = num_seqs * rows_per_seq.

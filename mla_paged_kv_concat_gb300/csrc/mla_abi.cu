@@ -113,26 +113,31 @@ bool pow2_block(int bs) {
   return bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256;
 }
 
-// SM count of the current device, queried once per device (calls from
-// several host threads may race to fill an entry; they store the same value).
-int device_sm_count() {
-  static std::atomic<int> cache[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  int n = cache[dev].load(std::memory_order_relaxed);
-  if (n == 0) {
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        n <= 0)
-      n = 148;
-    cache[dev].store(n, std::memory_order_relaxed);
-  }
-  return n;
-}
-
 // The tcgen05 kernel covers bf16 caches with a 512-wide latent.
 bool tc_supported(bool fp8, int R) { return !fp8 && R == 512; }
 
 }  // namespace
+
+namespace mla {
+
+cudaError_t device_sm_count(int* sms) {
+  static std::atomic<int> cache[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidDevice;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  *sms = n;
+  return cudaSuccess;
+}
+
+}  // namespace mla
 
 extern "C" {
 
@@ -162,8 +167,14 @@ size_t mla_decode_workspace_bytes(int num_rows, int num_heads,
   if (num_rows <= 0 || num_heads <= 0 || num_kv_splits <= 1 ||
       kv_lora_rank <= 0)
     return 0;
-  return static_cast<size_t>(num_rows) * num_heads * num_kv_splits *
-         (static_cast<size_t>(kv_lora_rank) + 1) * sizeof(float);
+  // rows * heads * splits * (R + 1) * 4, or SIZE_MAX when that does not fit
+  // a size_t (no workspace can be that large, so every caller refuses it)
+  size_t n = static_cast<size_t>(num_rows);
+  const size_t f[4] = {static_cast<size_t>(num_heads), static_cast<size_t>(num_kv_splits),
+                       static_cast<size_t>(kv_lora_rank) + 1, sizeof(float)};
+  for (size_t x : f)
+    if (__builtin_mul_overflow(n, x, &n)) return SIZE_MAX;
+  return n;
 }
 
 }  // extern "C"
@@ -413,7 +424,8 @@ mla_status build_stage1(const mla::DecodeParams& p_in, const void* kv_cache, boo
   s1->p = p_in;
   s1->fp8 = fp8;
   s1->R = R;
-  s1->sm_count = device_sm_count();
+  cudaError_t e = mla::device_sm_count(&s1->sm_count);
+  if (e != cudaSuccess) return cuda_fail(e);
   s1->tc = use_tc(s1->p, fp8, R, path);
   mla_status st = make_cache_tmap(&s1->tmap, kv_cache, fp8, R + 64, block_size, num_blocks,
                                   block_stride, 64);

@@ -12,12 +12,18 @@
 // The array is a file-scope __device__ variable, so every GPU that loads this
 // module holds kNoAllocBytes of it until the process exits.  In host code its
 // name is only a host-side stand-in, not a device address, so the device
-// address is looked up with cudaGetSymbolAddress, once per device, with that
-// device current, the first time this entry point runs on it.  Every call
-// shares the array: nothing in it has to start at zero (stage 1 writes every
-// partial the merge reads), but two calls whose kernels overlap on the GPU
-// (different streams, or different host threads on one device) race on it.
+// address is looked up with cudaGetSymbolAddress, once per device and
+// context, with that device current, the first time this entry point runs
+// there.  The address is cached together with the context's unique id: after
+// cudaDeviceReset (or any other end of the primary context) the module is
+// loaded again, perhaps at another address, and the next call looks the
+// address up again.  Every call shares the array: nothing in it has to start
+// at zero (stage 1 writes every partial the merge reads), but two calls whose
+// kernels overlap on the GPU (different streams, or different host threads
+// on one device) race on it.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include <mutex>
@@ -33,21 +39,53 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
+unsigned long long g_ctx_id[kMaxDevices] = {};
 
-// Device address of the array on the current device (looked up once).
+// Unique id of the current context (0 when the driver cannot say; then
+// the address is looked up on every call).
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the array on the current device and context.
 cudaError_t workspace_address(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_addr[dev]) {
-    void* p = nullptr;
+  // (with no context current yet the id is 0; cudaGetSymbolAddress then
+  // makes the device's primary context current and loads the module)
+  void* p = g_addr[dev];
+  const unsigned long long id = current_context_id();
+  if (!p || id == 0 || id != g_ctx_id[dev]) {
     e = cudaGetSymbolAddress(&p, g_noalloc_workspace);
     if (e != cudaSuccess) return e;
     g_addr[dev] = p;
+    g_ctx_id[dev] = current_context_id();
   }
-  *out = g_addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

@@ -78,6 +78,26 @@ def sample_pairs(w: W.Workload, n: int, seed: int = 0) -> np.ndarray:
     return np.stack([idx // w.num_heads, idx % w.num_heads], axis=1)
 
 
+def unit_pairs(w: W.Workload, unit: int, extra: int = 0, seed: int = 0) -> np.ndarray:
+    """(row, head) pairs that reach every unit of a stage-1 schedule: the
+    first and last query vector of each `unit`-vector block of each sequence
+    (a sequence's rows_per_seq * H vectors in row-major order), plus `extra`
+    random pairs."""
+    H = w.num_heads
+    nvec = w.rows_per_seq * H
+    flat = []
+    for b in range(w.num_seqs):
+        for g0 in range(0, nvec, unit):
+            for v in (g0, min(g0 + unit, nvec) - 1):
+                flat.append((b * w.rows_per_seq + v // H) * H + v % H)
+    if extra:
+        rng = np.random.default_rng(seed)
+        flat.extend(rng.choice(w.num_rows * H, size=min(extra, w.num_rows * H),
+                               replace=False).tolist())
+    idx = np.unique(np.asarray(flat, np.int64))
+    return np.stack([idx // H, idx % H], axis=1)
+
+
 def assert_close(o_gpu: torch.Tensor, lse_gpu: torch.Tensor, o_ref: np.ndarray,
                  lse_ref: np.ndarray, pairs=None, what=""):
     R = o_ref.shape[-1]

@@ -90,6 +90,24 @@ def test_split_rule_and_workspace_size(lib):
     assert mla.mla_decode_workspace_bytes(64, 16, 1, 512) == 0
 
 
+def test_workspace_size_overflow_is_refused(lib):
+    """A workspace size that does not fit a size_t reads as SIZE_MAX, so no
+    caller can pass a buffer that large and the no-alloc entry point refuses
+    the call before touching its fixed array (nothing is dereferenced)."""
+    size_max = (1 << 64) - 1
+    big = (2 ** 31 - 1, 128, 65535, 512)
+    assert (2 ** 31 - 1) * 128 * 65535 * 513 * 4 > size_max
+    assert mla.mla_decode_workspace_bytes(*big) == size_max
+    rows, H, S, R = big
+    st = lib.mla_decode_noalloc(FAKE, H * 576, 576, rows, H, FAKE, 0, 64, 64, 64 * 576, R, 64,
+                                FAKE, 1, 1, FAKE, 1, 0.1, None, S, FAKE, FAKE, None, None)
+    assert st == 3  # MLA_ERR_WORKSPACE_TOO_SMALL
+    st = lib.mla_decode(FAKE, H * 576, 576, rows, H, FAKE, 0, 64, 64, 64 * 576, R, 64,
+                        FAKE, 1, 1, FAKE, 1, 0.1, None, S, FAKE, size_max - 1, FAKE, FAKE,
+                        None, None)
+    assert st == 3
+
+
 def test_status_strings(lib):
     for code in range(5):
         assert lib.mla_status_string(code).decode().startswith("MLA_")

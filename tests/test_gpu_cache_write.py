@@ -127,7 +127,7 @@ def test_num_tokens_smaller_than_rows(cuda_dev):
     assert d.cache_numpy().tobytes() == oracle_cache(w).tobytes()
 
 
-@pytest.mark.parametrize("scale", [1.0, 0.05, 0.3, 7.0, 1e-30, 3e37])
+@pytest.mark.parametrize("scale", [1.0, 0.05, 0.3, 7.0, 1e-30, 3e37, 2.0 ** -130, 2.0 ** 127])
 def test_fp8_every_bf16_value(cuda_dev, scale):
     """Every finite bf16 bit pattern through the fp8 write, byte-exact against
     the oracle's IEEE division and E4M3 rounding (ties, subnormals, saturation,

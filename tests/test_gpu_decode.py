@@ -17,7 +17,7 @@ import mla_paged_kv_concat_gb300 as mla
 from mla_paged_kv_concat_gb300 import workloads as W
 
 from _helpers import (Dev, assert_close, oracle_cache, oracle_decode, sample_pairs,
-                      sm_count)
+                      sm_count, unit_pairs)
 
 pytestmark = pytest.mark.gpu
 
@@ -67,9 +67,12 @@ def test_per_shard_full(cuda_dev):
 
 @pytest.mark.slow
 def test_full_head_sampled(cuda_dev):
+    """B=128, H=128 at the benchmark's split count: the first and last query
+    vector of every (sequence, 128-vector) unit of the tcgen05 schedule, plus
+    random pairs."""
     w = W.make("full_head")
     S = mla.mla_num_kv_splits(w.max_seq_len, sm_count())
-    _run(w, S, pairs=sample_pairs(w, 48, seed=3))
+    _run(w, S, pairs=unit_pairs(w, 128, extra=32, seed=3))
 
 
 @pytest.mark.slow
@@ -82,7 +85,7 @@ def test_full_head_deterministic_single_pass(cuda_dev):
     o2, l2 = d.decode(1)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
-    pairs = sample_pairs(w, 24, seed=4)
+    pairs = unit_pairs(w, 128, extra=16, seed=4)
     o_ref, lse_ref = oracle_decode(w, oracle_cache(w), pairs=pairs)
     assert_close(o1, l1, o_ref, lse_ref, pairs=pairs, what="full_head S=1")
 
@@ -90,14 +93,18 @@ def test_full_head_deterministic_single_pass(cuda_dev):
 def test_fp8_small(cuda_dev):
     w = W.make("fp8_small")
     S = mla.mla_num_kv_splits(w.max_seq_len, sm_count())
-    _run(w, S, pairs=sample_pairs(w, 96, seed=5))
+    # every (sequence, 32-vector) unit of the warp-MMA schedule, plus random pairs
+    _run(w, S, pairs=unit_pairs(w, 32, extra=64, seed=5))
 
 
 @pytest.mark.slow
 def test_long_multirow_sampled(cuda_dev):
+    """8 sequences x 4 rows x 128 heads at the benchmark's split count: the
+    first and last vector of each of the 32 (sequence, 128-vector) units of
+    the chunked tcgen05 schedule, plus random pairs."""
     w = W.make("long_multirow")
     S = mla.mla_num_kv_splits(w.max_seq_len, sm_count())
-    _run(w, S, pairs=sample_pairs(w, 12, seed=6))
+    _run(w, S, pairs=unit_pairs(w, 128, extra=8, seed=6))
 
 
 SMALL = [
@@ -309,7 +316,7 @@ def test_split_count_at_its_cap(cuda_dev, path):
                         pool_blocks=2600)
     S = mla.mla_num_kv_splits(w.max_seq_len, sm_count())
     assert S == 2 * sm_count()
-    pairs = None if H == 16 else sample_pairs(w, 48, seed=8)
+    pairs = None if H == 16 else unit_pairs(w, 128, extra=32, seed=8)
     d, o, lse = _run(w, S, path, pairs=pairs)
     assert int(d.err.item()) == 0
 

@@ -39,7 +39,7 @@ def _write(d):
                     scale=d.kv_scale, err_count=d.err)
 
 
-@pytest.mark.parametrize("scale", [1.0, 0.05, 3.0, 1e-30, 3e37])
+@pytest.mark.parametrize("scale", [1.0, 0.05, 3.0, 1e-30, 3e37, 2.0 ** -130, 2.0 ** 127])
 def test_e5m2_every_bf16_value(cuda_dev, scale):
     R, P = 256, 64
     D = R + P

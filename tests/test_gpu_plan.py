@@ -171,13 +171,15 @@ def test_plan_graph_replay_over_new_contents(cuda_dev, H, fused, pair):
     plan.close()
 
 
-@pytest.mark.parametrize("name,npairs", [("per_shard", 128), ("full_head", 32)])
-def test_benchmark_configuration_through_a_plan(cuda_dev, name, npairs):
+@pytest.mark.parametrize("name,unit", [("per_shard", 16), ("full_head", 128),
+                                       ("long_multirow", 128)])
+def test_benchmark_configuration_through_a_plan(cuda_dev, name, unit):
     """The benchmark's step as it times it: one plan over the resident
     tensors (write of the new tokens, stage 1 at the rule's split count,
-    merge), run once; the cache compared byte for byte and sampled (row, head)
-    outputs against the oracle."""
-    from _helpers import sample_pairs
+    merge), run once; the cache compared byte for byte and, against the
+    oracle, the first and last (row, head) of every stage-1 unit (`unit`
+    query vectors of one sequence) plus random pairs."""
+    from _helpers import unit_pairs
     w = W.make(name)
     d = _device(w)
     S = mla.mla_num_kv_splits(w.max_seq_len, sm_count())
@@ -190,6 +192,6 @@ def test_benchmark_configuration_through_a_plan(cuda_dev, name, npairs):
     assert int(d.err.item()) == 0
     cache = oracle_cache(w)
     assert d.cache_numpy().tobytes() == cache.tobytes()
-    pairs = sample_pairs(w, npairs, seed=11)
+    pairs = unit_pairs(w, unit, extra=32, seed=11)
     o_ref, lse_ref = oracle_decode(w, cache, pairs=pairs)
     assert_close(o, lse, o_ref, lse_ref, pairs=pairs, what=f"{name} through a plan")

@@ -74,3 +74,19 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2
     assert rec["value"] > 0 and rec["cpu_baseline"]["kind"] == "oracle"
     assert rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_gpus_flag_without_a_launcher_starts_that_many_ranks():
+    """`bench.py --gpus 2` run directly (the form the scaling run uses
+    without torchrun) relaunches itself under torch.distributed.run with two
+    processes; the reference arm's single line then reports both ranks."""
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--gpus", "2",
+           "--steps", "1", "--warmup", "3", "--ref-rows", "2"]
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2
