@@ -121,26 +121,268 @@ __device__ __forceinline__ uint8_t quant1(uint16_t bits, float s) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// RMSNorm of 8 latent elements: bf16(x * inv * gamma).
-__device__ __forceinline__ uint4 norm8(uint4 x, uint4 g, float inv) {
+// ---------------------------------------------------------------------------
+// Exact rounding of the fused write's results.
+//
+// The reference result of the RMSNorm and of the rotation is their fp64
+// evaluation rounded once to bf16 (nearest, ties to even).  The kernel gets
+// the same bits without evaluating fp64 on every element (fp64 is slow on
+// this GPU).  bf16 rounding is monotone and changes only at the midpoints
+// between consecutive bf16 values; whenever a computed value and a bound on
+// its distance from the exact result show that no midpoint lies between
+// them, the exact result, its fp64 evaluation (within 2^-44 relative of it
+// for the RMSNorm, 2^-53 for the rotation) and the computed value round to
+// the same bf16 value.  Three tiers:
+//   1. fp32, as a plain evaluation would do it, with a bound of a few units
+//      in the last place (ulp): decided unless the value lies within that
+//      many ulps of a midpoint (about one element in 4000);
+//   2. for those, double-float (an unevaluated sum h + lo of two fp32
+//      values) with a bound near 2^-40 relative: decided unless the exact
+//      result is practically on the midpoint (exact ties);
+//   3. the rest in fp64, in the reference's operation order, every
+//      operation correctly rounded, then rounded to bf16.
+// Inputs outside the range where the bounds hold (NaN, infinities, results
+// below 2^-100 or above 2^126, rows whose magnitudes span more than 2^100)
+// go to the later tiers as well.  Tiers 2 and 3 are separate, non-inlined
+// functions behind branches that are rarely taken, so that their
+// instructions are not issued on the common path.
+
+// s + e = a + b exactly (Knuth's two-sum; no ordering of |a|, |b| needed).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// fp64 -> bf16 bits, round to nearest, ties to even; any NaN -> 0x7FC0;
+// results of 2^128 and above are infinities.
+__device__ __forceinline__ uint32_t bf16_from_f64(double y) {
+  const uint64_t u = static_cast<uint64_t>(__double_as_longlong(y));
+  const uint32_t sign = static_cast<uint32_t>(u >> 48) & 0x8000u;
+  const uint64_t a = u & 0x7FFFFFFFFFFFFFFFull;
+  if (a > 0x7FF0000000000000ull) return 0x7FC0u;
+  if (a >= 0x47F0000000000000ull) return sign | 0x7F80u;  // |y| >= 2^128
+  if (a >= 0x3810000000000000ull) {                       // |y| >= 2^-126
+    // keep 7 of the 52 fraction bits; the carry of the rounding increment
+    // runs into the exponent field
+    const uint64_t r = (a + 0x00000FFFFFFFFFFFull + ((a >> 45) & 1u)) >> 45;
+    const uint64_t bits = r - (static_cast<uint64_t>(1023 - 127) << 7);
+    return bits >= 0x7F80u ? (sign | 0x7F80u) : (sign | static_cast<uint32_t>(bits));
+  }
+  // below 2^-126: multiples of 2^-133 (|y| * 2^133 is exact and below 2^7;
+  // rint rounds to nearest even; 128 is the smallest normal, 0x0080)
+  const double n = rint(fabs(y) * 0x1p133);
+  return sign | static_cast<uint32_t>(n);
+}
+
+// Tier 1 test on two values y0, y1, each known to lie within d0 (d1) of its
+// exact result: both ends of each bracket [y - d, y + d] round to the same
+// bf16 value (round to nearest even; rounding is monotone, so the exact
+// result rounds there too), and that value is finite (an infinity or NaN
+// here comes from an fp32 overflow or a non-finite input, which the fp64
+// evaluation may treat differently).  On success *r holds the two bf16 values
+// (y0 low).  Three conversions' worth of work per pair instead of a
+// per-element distance test.
+__device__ __forceinline__ bool bracket2(float y0, float d0, float y1, float d1, uint32_t& r) {
+  const uint32_t lo = pack_bf16x2(y0 - d0, y1 - d1);
+  const uint32_t hi = pack_bf16x2(y0 + d0, y1 + d1);
+  r = lo;
+  // a half whose exponent bits are all ones gets bit 15 set by the add
+  const uint32_t nonfinite = ((lo & 0x7F807F80u) + 0x00800080u) & 0x80008000u;
+  return lo == hi && nonfinite == 0u;
+}
+
+// Tier 2 rounding: y to bf16 from y ~= h + lo, |y - (h + lo)| <= B, when no
+// bf16 midpoint lies within B of h + lo; false otherwise (and for h outside
+// [2^-100, 2^126] in magnitude, where the callers' bounds stop).
+__device__ __forceinline__ bool round_bf16_df(float h, float lo, float B, uint32_t& out) {
+  const float ah = fabsf(h);
+  if (!(ah >= 0x1p-100f && ah <= 0x1p126f)) return false;
+  const uint32_t u = __float_as_uint(h);
+  const uint32_t t = u & 0x7FFF0000u;  // |h| truncated to bf16
+  // distance from the midpoint above t (same binade as |h|, so ah - mid is
+  // exact), corrected by lo in the direction of |h|
+  const float d = (ah - __uint_as_float(t | 0x8000u)) + ((u >> 31) ? -lo : lo);
+  if (!(fabsf(d) > B)) return false;
+  out = ((u >> 16) & 0x8000u) | ((t >> 16) + (d > 0.f ? 1u : 0u));
+  return true;
+}
+
+__device__ __forceinline__ float bfv(uint32_t w, int hi) {
+  return hi ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+}
+
+// Per-token terms of the RMSNorm: x / sqrt(mean x^2 + eps) * gamma is
+// computed as (x sc) gamma inv with sc = 2^-k (k the binade of the row's
+// largest element, so that the scaled squares and their sum stay in range)
+// and inv = 1 / sqrt(mean (x sc)^2 + eps sc^2) ~= inv32 + inv_lo.  Error
+// budget: the scaled sum of squares is accumulated with two-sum (exact high
+// part, low parts in fp32), within 2^-39 of the exact sum (the reference's
+// sequential fp64 sum is within (R - 1) 2^-53 < 2^-44 of it); one Newton
+// step on rsqrtf (error below 2^-21) leaves inv32 + inv_lo within 2^-39.5 of
+// inv, and inv32, its rounding to fp32, within 2^-24 + 2^-39.5.  Since the
+// largest scaled element is at least 1, the mean is at least 2^-9 and
+// inv <= 2^4.5, so sc inv32 <= 2^24.5 for the tokens that take tier 1
+// (k >= -20).
+struct NormTerms {
+  float sc, inv32, inv_lo;
+  bool fast;  // false: every element takes the fp64 path
+};
+
+// Tier 1 of the RMSNorm for 8 elements: p = RN(xg inv_s), xg = x gamma
+// (exact: two 8-bit significands; within 2^-150 if it underflows) and
+// inv_s = sc inv32 (a power-of-two scaling of inv32, exact), is within
+// 2^-23 |y| (1 + 2^-15) + 2^-125 of y (the absolute part covers a subnormal
+// xg, inv_s being at most 2^24.5 on the tokens that take this tier); the
+// bracket is 2^-20 |p| + 2^-120.  Bit 2i (pair i, both halves) of *need is
+// set for each pair left to tier 2.
+__device__ __forceinline__ uint4 norm8(uint4 x, uint4 g, float inv_s, uint32_t& need) {
   const uint32_t xv[4] = {x.x, x.y, x.z, x.w}, gv[4] = {g.x, g.y, g.z, g.w};
   uint32_t o[4];
+  need = 0;
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-    o[k] = pack_bf16x2(bf_lo(xv[k]) * inv * bf_lo(gv[k]), bf_hi(xv[k]) * inv * bf_hi(gv[k]));
+  for (int k = 0; k < 4; ++k) {
+    const float p0 = (bfv(xv[k], 0) * bfv(gv[k], 0)) * inv_s;
+    const float p1 = (bfv(xv[k], 1) * bfv(gv[k], 1)) * inv_s;
+    const float d0 = fmaf(fabsf(p0), 0x1p-20f, 0x1p-120f);
+    const float d1 = fmaf(fabsf(p1), 0x1p-20f, 0x1p-120f);
+    if (!bracket2(p0, d0, p1, d1, o[k])) need |= 3u << (2 * k);
+  }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Tier 2 of the RMSNorm for the elements flagged in `need`: p + lo with
+// p = RN(xg inv32), its exact error (fma) and xg inv_lo, within 2^-38 |y| of
+// y; the bound used is 2^-36 |p|.  Elements it cannot decide are flagged in
+// *fb for tier 3.
+__device__ __noinline__ uint4 norm8_df(uint4 x, uint4 g, float sc, float inv32, float inv_lo,
+                                       uint4 cur, uint32_t need, uint32_t* fb) {
+  const uint32_t xv[4] = {x.x, x.y, x.z, x.w}, gv[4] = {g.x, g.y, g.z, g.w};
+  uint32_t o[4] = {cur.x, cur.y, cur.z, cur.w};
+  uint32_t f = 0;
+  for (int i = 0; i < 8; ++i) {
+    if (!(need & (1u << i))) continue;
+    const int k = i >> 1, j = i & 1;
+    const float xs = bfv(xv[k], j) * sc;
+    const float xg = xs * bfv(gv[k], j);
+    const float p = xg * inv32;
+    const float lo = fmaf(xg, inv_lo, fmaf(xg, inv32, -p));
+    uint32_t r = 0;
+    if (fabsf(xs) >= 0x1p-126f && round_bf16_df(p, lo, fabsf(p) * 0x1p-36f, r))
+      o[k] = j ? ((o[k] & 0xFFFFu) | (r << 16)) : ((o[k] & 0xFFFF0000u) | r);
+    else
+      f |= 1u << i;
+  }
+  *fb = f;
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Tier 3 of the RMSNorm for the elements flagged in fb: (x * inv) * gamma in
+// fp64, inv the reference's fp64 1 / sqrt(ss / R + eps).
+__device__ __noinline__ uint4 norm8_f64(uint4 x, uint4 g, double inv, uint4 cur,
+                                        uint32_t fb) {
+  const uint32_t xv[4] = {x.x, x.y, x.z, x.w}, gv[4] = {g.x, g.y, g.z, g.w};
+  uint32_t o[4] = {cur.x, cur.y, cur.z, cur.w};
+  for (int i = 0; i < 8; ++i) {
+    if (!(fb & (1u << i))) continue;
+    const int k = i >> 1, j = i & 1;
+    const double y = __dmul_rn(__dmul_rn(static_cast<double>(bfv(xv[k], j)), inv),
+                               static_cast<double>(bfv(gv[k], j)));
+    const uint32_t r = bf16_from_f64(y);
+    o[k] = j ? ((o[k] & 0xFFFFu) | (r << 16)) : ((o[k] & 0xFFFF0000u) | r);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The reference's fp64 1 / sqrt(ss / R + eps), ss summed in element order
+// from the row in memory (one thread).
+__device__ __noinline__ double rms_inv_f64(const uint16_t* row, int R, float eps) {
+  const uint4* src = reinterpret_cast<const uint4*>(row);
+  double ss = 0.0;
+  for (int c = 0; c < R / 8; ++c) {
+    const uint4 w4 = __ldg(src + c);
+    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+    for (int e = 0; e < 8; ++e) {
+      const double xd = bfv(wv[e >> 1], e & 1);
+      ss = __dadd_rn(ss, __dmul_rn(xd, xd));
+    }
+  }
+  const double ms = __ddiv_rn(ss, static_cast<double>(R));
+  return __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(ms, static_cast<double>(eps))));
+}
+
+// Tier 2 of one rotated value.  Double-float: both products split exactly
+// into value + error (fma), their sum by two-sum, the errors added in fp32,
+// the pair renormalised by a second two-sum (under cancellation the error
+// terms can be as large as the result): within 2^-45 (|u c| + |v s|) of the
+// exact result; the bound used is 2^-40 (|u c| + |v s|).  Products outside
+// [2^-100, 2^126] (unless exactly zero from a zero factor) are left to
+// tier 3, as are results next to a midpoint.
+__device__ __forceinline__ bool rot1_df(float u, float c, float v, float s, float sgn,
+                                        uint32_t& r) {
+  const float p1 = u * c, p2 = sgn * (v * s);
+  const float a1 = fabsf(p1), a2 = fabsf(p2);
+  const bool in1 = (a1 >= 0x1p-100f && a1 <= 0x1p126f) || (p1 == 0.f && (u == 0.f || c == 0.f));
+  const bool in2 = (a2 >= 0x1p-100f && a2 <= 0x1p126f) || (p2 == 0.f && (v == 0.f || s == 0.f));
+  if (!(in1 && in2)) return false;
+  const float e1 = fmaf(u, c, -p1);
+  const float e2 = fmaf(sgn * v, s, -p2);
+  float h, t, lo;
+  two_sum(p1, p2, h, t);
+  two_sum(h, t + (e1 + e2), h, lo);
+  if (h == 0.f && lo == 0.f) {
+    // exact zero (p1 = -p2 and no product error): the fp64 sum is +0
+    // unless both terms are -0
+    r = (__float_as_uint(p1) & __float_as_uint(p2)) == 0x80000000u ? 0x8000u : 0u;
+    return true;
+  }
+  return round_bf16_df(h, lo, (a1 + a2) * 0x1p-40f, r);
+}
+
 // Non-NeoX rotation of 4 interleaved pairs (8 bf16) by angles with the given
-// cos and sin: (a, b) -> (a c - b s, b c + a s), rounded to bf16.
-__device__ __forceinline__ uint4 rope8(uint4 x, float4 c, float4 s) {
+// cos and sin: (a, b) -> (a c - b s, b c + a s), tier 1: y = fma(a, c, p2)
+// with p2 = RN(-b s) (or fma(b, c, RN(a s))) is within 2^-24 (|p2| + |y|)
+// + 2^-149 of the exact result (the product inside the fma is exact); the
+// bracket is 2^-22 (|p2| + |y|) + 2^-120.  Bit i of *need is set for each
+// element i left to tier 2 (both elements of a pair together).
+__device__ __forceinline__ uint4 rope8(uint4 x, float4 c, float4 s, uint32_t& need) {
   const uint32_t xv[4] = {x.x, x.y, x.z, x.w};
   const float cv[4] = {c.x, c.y, c.z, c.w}, sv[4] = {s.x, s.y, s.z, s.w};
   uint32_t o[4];
+  need = 0;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float a = bf_lo(xv[k]), b = bf_hi(xv[k]);
-    o[k] = pack_bf16x2(a * cv[k] - b * sv[k], b * cv[k] + a * sv[k]);
+    const float a = bfv(xv[k], 0), b = bfv(xv[k], 1);
+    const float q0 = -(b * sv[k]), q1 = a * sv[k];
+    const float y0 = fmaf(a, cv[k], q0), y1 = fmaf(b, cv[k], q1);
+    const float d0 = fmaf(fabsf(q0) + fabsf(y0), 0x1p-22f, 0x1p-120f);
+    const float d1 = fmaf(fabsf(q1) + fabsf(y1), 0x1p-22f, 0x1p-120f);
+    if (!bracket2(y0, d0, y1, d1, o[k])) need |= 3u << (2 * k);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Tiers 2 and 3 of the rotation for the elements flagged in `need`: the
+// double-float value, and where it cannot decide, fp64 (products exact in
+// fp64, one rounding for the sum, then one to bf16).
+__device__ __noinline__ uint4 rope8_slow(uint4 x, float4 c, float4 s, uint4 cur,
+                                         uint32_t need) {
+  const uint32_t xv[4] = {x.x, x.y, x.z, x.w};
+  const float cv[4] = {c.x, c.y, c.z, c.w}, sv[4] = {s.x, s.y, s.z, s.w};
+  uint32_t o[4] = {cur.x, cur.y, cur.z, cur.w};
+  for (int i = 0; i < 8; ++i) {
+    if (!(need & (1u << i))) continue;
+    const int k = i >> 1, j = i & 1;
+    // j = 0: a c - b s; j = 1: b c + a s
+    const float u = bfv(xv[k], j), v = bfv(xv[k], j ^ 1);
+    const float sgn = j ? 1.f : -1.f;
+    uint32_t r;
+    if (!rot1_df(u, cv[k], v, sv[k], sgn, r)) {
+      const double pu = __dmul_rn(static_cast<double>(u), static_cast<double>(cv[k]));
+      const double pv = __dmul_rn(static_cast<double>(v), static_cast<double>(sv[k]));
+      r = bf16_from_f64(j ? __dadd_rn(pu, pv) : __dsub_rn(pu, pv));
+    }
+    o[k] = j ? ((o[k] & 0xFFFFu) | (r << 16)) : ((o[k] & 0xFFFF0000u) | r);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
@@ -217,27 +459,108 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NR ? 3 : 1)
           if (lane == 0 && a.err_count) atomicAdd(a.err_count, 1);
           continue;  // the whole token is skipped
         }
-        float ss = 0.f;
+        // ---- RMSNorm terms (see NormTerms): the largest binade k of the
+        // row, the scaled sum of squares as a two-sum pair, 1 / sqrt(t)
+        NormTerms nt;
+        {
+          uint32_t ebits = 0;  // largest bf16 exponent field of this lane's elements
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if (lane + 32 * k < nc) {
+              const uint32_t xv[4] = {v[0][k].x, v[0][k].y, v[0][k].z, v[0][k].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                ebits = max(ebits, max((xv[e] >> 7) & 0xFFu, (xv[e] >> 23) & 0xFFu));
+            }
+          }
+          const int kexp = static_cast<int>(__reduce_max_sync(0xffffffffu, ebits)) - 127;
+          // all-zero or subnormal-only rows, NaN or infinity (field 0xFF), or a
+          // binade too far from 1 take the fp64 path
+          nt.fast = kexp >= -20 && kexp <= 100;
+          nt.sc = __uint_as_float(static_cast<uint32_t>(127 - (nt.fast ? kexp : 0)) << 23);
+          float sh = 0.f, sl = 0.f;
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if (lane + 32 * k < nc) {
+              const uint32_t xv[4] = {v[0][k].x, v[0][k].y, v[0][k].z, v[0][k].w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float xs = bfv(xv[e >> 1], e & 1) * nt.sc;
+                float err;
+                two_sum(sh, xs * xs, sh, err);  // xs^2 exact above 2^-126
+                sl += err;
+              }
+            }
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const float oh = __shfl_xor_sync(0xffffffffu, sh, o);
+            const float ol = __shfl_xor_sync(0xffffffffu, sl, o);
+            float err;
+            two_sum(sh, oh, sh, err);
+            sl += ol + err;
+          }
+          // one value for the whole warp (lanes summed in different orders)
+          sh = __shfl_sync(0xffffffffu, sh, 0);
+          sl = __shfl_sync(0xffffffffu, sl, 0);
+          const float rinv = 1.0f / static_cast<float>(a.R);  // a power of two: exact
+          const float eps_s = a.eps * nt.sc * nt.sc;
+          float th, tl;
+          two_sum(sh * rinv, eps_s, th, tl);
+          tl += sl * rinv;
+          {
+            const float h2 = th + tl;  // renormalise (|tl| << |th|)
+            tl = tl - (h2 - th);
+            th = h2;
+          }
+          nt.fast = nt.fast && eps_s <= 0x1p100f && th >= 0x1p-100f && th <= 0x1p100f;
+          // Newton step on rsqrtf in double-float: e = 1 - t r0^2, inv =
+          // r0 (1 + e/2 + 3e^2/8)
+          const float r0 = rsqrtf(th);
+          const float q2 = r0 * r0, q2l = fmaf(r0, r0, -q2);
+          const float m = th * q2, ml = fmaf(th, q2, -m);
+          const float e = ((1.0f - m) - ml) - fmaf(th, q2l, tl * q2);
+          two_sum(r0, r0 * (e * fmaf(0.375f, e, 0.5f)), nt.inv32, nt.inv_lo);
+        }
+        // tier 1's scale: inv32 scaled back by sc (exact while normal)
+        const float inv_s = nt.sc * nt.inv32;
+        if (!(inv_s >= 0x1p-100f)) nt.fast = false;
+        // Tier 1 for the latent chunks (0, 1) and the rope chunk (2); tier 2
+        // for the elements it leaves; fbm: elements left to tier 3
+        uint32_t fbm[3] = {0u, 0u, 0u};
+        uint4 kpe_in = make_uint4(0, 0, 0, 0);
+        const uint16_t* row = a.kv_c + static_cast<int64_t>(t) * a.kv_c_stride;
 #pragma unroll
         for (int k = 0; k < 3; ++k) {
           const int c = lane + 32 * k;
           if (c < nc) {
-            const uint32_t xv[4] = {v[0][k].x, v[0][k].y, v[0][k].z, v[0][k].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              ss += bf_lo(xv[e]) * bf_lo(xv[e]) + bf_hi(xv[e]) * bf_hi(xv[e]);
+            if (k < 2) {
+              uint32_t need;
+              const uint4 xin = v[0][k];
+              v[0][k] = norm8(xin, gm[k], inv_s, need);
+              if (!nt.fast)
+                fbm[k] = 0xFFu;
+              else if (need)
+                v[0][k] = norm8_df(xin, gm[k], nt.sc, nt.inv32, nt.inv_lo, v[0][k], need,
+                                   &fbm[k]);
+            }
+          } else if (c < nc + np) {
+            uint32_t need;
+            kpe_in = v[0][k];
+            v[0][k] = rope8(kpe_in, cv, sv, need);
+            if (need) v[0][k] = rope8_slow(kpe_in, cv, sv, v[0][k], need);
           }
         }
+        if (__any_sync(0xffffffffu, (fbm[0] | fbm[1]) != 0u)) {
+          // tier 3: the reference's fp64 1 / sqrt(ss / R + eps), from lane 0
+          double inv64 = 0.0;
+          if (lane == 0) inv64 = rms_inv_f64(row, a.R, a.eps);
+          inv64 = __shfl_sync(0xffffffffu, inv64, 0);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float inv = __frsqrt_rn(ss * (1.0f / static_cast<float>(a.R)) + a.eps);
-#pragma unroll
-        for (int k = 0; k < 3; ++k) {
-          const int c = lane + 32 * k;
-          if (c < nc)
-            v[0][k] = norm8(v[0][k], gm[k < 2 ? k : 0], inv);
-          else if (c < nc + np)
-            v[0][k] = rope8(v[0][k], cv, sv);
+          for (int k = 0; k < 2; ++k)
+            if (fbm[k])
+              v[0][k] = norm8_f64(__ldg(reinterpret_cast<const uint4*>(row) + lane + 32 * k),
+                                  gm[k], inv64, v[0][k], fbm[k]);
         }
         if (a.q_pe != nullptr) {
           // q_pe of this token: q_heads x 8 chunks, chunk lane + 32 i is
@@ -253,12 +576,21 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, NR ? 3 : 1)
                 x[u] = *reinterpret_cast<const uint4*>(qrow + (c >> 3) * a.q_pe_head_stride +
                                                        (c & 7) * 8);
             }
+            uint4 y[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (c0 + 32 * u + lane < nq) {
+                uint32_t need;
+                y[u] = rope8(x[u], cv, sv, need);
+                if (need) y[u] = rope8_slow(x[u], cv, sv, y[u], need);
+              }
+            }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int c = c0 + 32 * u + lane;
               if (c < nq)
                 *reinterpret_cast<uint4*>(qrow + (c >> 3) * a.q_pe_head_stride + (c & 7) * 8) =
-                    rope8(x[u], cv, sv);
+                    y[u];
             }
           }
         }
