@@ -162,15 +162,17 @@ def _roofline(w, args, workload, deterministic, kv_bytes, flops, s1_ms):
     hbm, bf16, src = _peaks()
     R, H = w.kv_lora_rank, w.num_heads
     achieved = kv_bytes / (s1_ms * 1e-3) / 1e9
-    # the stage-1 kernel the library picks (tcgen05 for bf16, R = 512 and at
-    # least 128 query vectors per sequence; warp MMA otherwise)
-    tc = (not w.kv_fp8) and R == 512 and w.rows_per_seq * H >= 128 and args.path != 1
+    # the stage-1 kernel the library picks: a tcgen05 kernel (R = 512 bf16:
+    # CTA pairs; R = 256 bf16 or fp8: one CTA) from 64 query vectors per
+    # sequence, warp MMA otherwise
+    tc = (R == 256 or not w.kv_fp8) and w.rows_per_seq * H >= 64 and args.path != 1
     tc = tc or args.path == 2
-    kernel_src = "decode_tc.cu" if tc else "decode_mma.cu"
+    kernel_src = ("decode_tc1.cu" if R == 256 else "decode_tc.cu") if tc else "decode_mma.cu"
     traffic = _traffic_record(os.path.join(ROOT, "mla_paged_kv_concat_gb300", "csrc",
                                            kernel_src),
                               workload + ("_s1" if deterministic else ""))
-    kname = ("decode_tc_kernel" if tc else "decode_mma_kernel") + " (stage 1)"
+    kname = (("decode_tc1_kernel" if R == 256 else "decode_tc_kernel") if tc
+             else "decode_mma_kernel") + " (stage 1)"
     if flops / (bf16 * 1e12) > kv_bytes / (hbm * 1e9):
         # above the ridge (several query rows share each cached row): the
         # contraction's flops against the bf16 tensor peak

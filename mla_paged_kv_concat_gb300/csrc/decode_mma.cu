@@ -66,9 +66,14 @@ struct MmaCfg {
   static constexpr int QBYTES = NCH * QBOX;
   static constexpr int PPITCH = kBN + 8;        // P row pitch (elements)
   static constexpr int PBYTES = 16 * MT * PPITCH * 2;
+  // fp8 with R = 256: two converted tiles, so that the conversion of tile
+  // n + 1 runs between the S products of tile n (software pipelining); the
+  // 576-wide fp8 tiles leave room for one
+  static constexpr bool PIPE = FP8 && R == 256;
+  static constexpr int NCONV = FP8 ? (PIPE ? 2 : 1) : 0;
   static constexpr int OFF_STAGES = 0;
   static constexpr int OFF_CONV = STAGES * STAGE_BYTES;
-  static constexpr int OFF_Q = OFF_CONV + (FP8 ? TILE : 0);  // two Q buffers
+  static constexpr int OFF_Q = OFF_CONV + NCONV * TILE;  // two Q buffers
   static constexpr int OFF_P = OFF_Q + 2 * QBYTES;
   static constexpr int OFF_RED = OFF_P + PBYTES;
   static constexpr int RED_BYTES = 2 * MT * 4 * 16 * 4;
@@ -98,6 +103,26 @@ __device__ __forceinline__ void fp8x16_to_bf16(uint4 raw, bool e5m2, uint4& lo,
   }
   lo = make_uint4(out[0], out[1], out[2], out[3]);
   hi = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
+// Converts 64-dim chunks [c_lo, c_hi) of a raw fp8 tile (64 rows of 64
+// bytes per chunk) into a bf16 tile (64 rows of 128 bytes per chunk,
+// 128-byte swizzled); rows at or past `valid` become zeros.  Thread `ctid`
+// of `nthreads` takes every nthreads-th 16-byte piece.
+__device__ __forceinline__ void convert_chunks(const uint8_t* raw, uint8_t* conv, int c_lo,
+                                               int c_hi, int valid, bool e5m2, int ctid,
+                                               int nthreads) {
+  const int n = (c_hi - c_lo) * kBN * 4;
+  for (int i = ctid; i < n; i += nthreads) {
+    const int c = c_lo + i / (kBN * 4), r = (i >> 2) % kBN, kq = i & 3;
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+    if (r < valid)
+      fp8x16_to_bf16(*reinterpret_cast<const uint4*>(raw + c * (kBN * 64) + r * 64 + kq * 16),
+                     e5m2, lo, hi);
+    uint8_t* dst = conv + c * (kBN * 128);
+    *reinterpret_cast<uint4*>(dst + sw128(r, 2 * kq)) = lo;
+    *reinterpret_cast<uint4*>(dst + sw128(r, 2 * kq + 1)) = hi;
+  }
 }
 
 __device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
@@ -518,30 +543,49 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
     for (int n = 0; n < NT; ++n)
       acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 
+    if constexpr (C::PIPE) {
+      // the segment's first tile is converted here; every later one during
+      // the S products of the tile before it
+      if (sg.t_lo < sg.t_hi) {
+        const int st = it % STAGES;
+        if (!mbar_wait(&bar_full[st], (it / STAGES) & 1)) {
+          if (lane == 0 && p.err_count) atomicAdd(p.err_count, kTimeoutErr);
+          return false;
+        }
+        named_bar_sync(1, NCW * 32);  // the buffer's previous tile has been read
+        convert_chunks(s_stage + st * C::STAGE_BYTES, s_conv + (it & 1) * C::TILE, 0, NCH,
+                       min(kBN, sg.L - sg.t_lo * kBN), p.kv_e5m2 != 0, ctid, NCW * 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_empty[st]);
+        named_bar_sync(1, NCW * 32);
+      }
+    }
     for (int t = sg.t_lo; t < sg.t_hi; ++t, ++it) {
       const int st = it % STAGES;
       const uint32_t ph = (it / STAGES) & 1;
       const int valid = min(kBN, sg.L - t * kBN);
-      if (!mbar_wait(&bar_full[st], ph)) {
-        if (lane == 0 && p.err_count) atomicAdd(p.err_count, kTimeoutErr);
-        return false;
+      // pipelined fp8: the next tile of the segment is converted during this
+      // tile's S products (its raw stage must have landed first)
+      const bool pf = C::PIPE && t + 1 < sg.t_hi;
+      const int st_n = (it + 1) % STAGES;
+      const int valid_n = min(kBN, sg.L - (t + 1) * kBN);
+      uint8_t* conv_n = s_conv + ((it + 1) & 1) * C::TILE;
+      if (!C::PIPE || pf) {
+        const int wst = C::PIPE ? st_n : st;
+        const uint32_t wph = C::PIPE ? ((it + 1) / STAGES) & 1 : ph;
+        if (!mbar_wait(&bar_full[wst], wph)) {
+          if (lane == 0 && p.err_count) atomicAdd(p.err_count, kTimeoutErr);
+          return false;
+        }
       }
       uint8_t* tile;
-      if constexpr (FP8) {
+      if constexpr (C::PIPE) {
+        tile = s_conv + (it & 1) * C::TILE;
+      } else if constexpr (FP8) {
         // All warps are done reading the previous converted tile.
         named_bar_sync(1, NCW * 32);
-        const uint8_t* raw = s_stage + st * C::STAGE_BYTES;
-        for (int idx = ctid; idx < NCH * kBN * 4; idx += NCW * 32) {
-          const int c = idx / (kBN * 4), r = (idx >> 2) % kBN, kq = idx & 3;
-          uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-          if (r < valid)
-            fp8x16_to_bf16(
-                *reinterpret_cast<const uint4*>(raw + c * (kBN * 64) + r * 64 + kq * 16),
-                p.kv_e5m2 != 0, lo, hi);
-          uint8_t* dst = s_conv + c * (kBN * 128);
-          *reinterpret_cast<uint4*>(dst + sw128(r, 2 * kq)) = lo;
-          *reinterpret_cast<uint4*>(dst + sw128(r, 2 * kq + 1)) = hi;
-        }
+        convert_chunks(s_stage + st * C::STAGE_BYTES, s_conv, 0, NCH, valid, p.kv_e5m2 != 0,
+                       ctid, NCW * 32);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_empty[st]);
         named_bar_sync(1, NCW * 32);
@@ -580,6 +624,10 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
         const uint32_t b_kc = j & 1;
 #pragma unroll
         for (int c64 = 0; c64 < NCH; ++c64) {
+          // pipelined fp8: chunk c64 of the next tile, between the products
+          if (pf)
+            convert_chunks(s_stage + st_n * C::STAGE_BYTES, conv_n, c64, c64 + 1, valid_n,
+                           p.kv_e5m2 != 0, ctid, NCW * 32);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t kc = kk * 2;
@@ -589,6 +637,10 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
             mma_bf16_16816(ch[kk][0], a0, a1, a2, a3, b0, b1);
             mma_bf16_16816(ch[kk][1], a0, a1, a2, a3, b2, b3);
           }
+        }
+        if (pf) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_empty[st_n]);  // the raw stage is converted
         }
 #pragma unroll
         for (int jn = 0; jn < 2; ++jn)
@@ -694,6 +746,9 @@ __global__ void __launch_bounds__(MmaCfg<R, FP8, MT>::NTHREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_empty[st]);
       }
+      // pipelined fp8: every warp has read this tile's buffer and written
+      // its part of the next tile's before the next tile starts
+      if constexpr (C::PIPE) named_bar_sync(1, NCW * 32);
     }
 
     // ---- segment epilogue: normalise and write (final o/lse, or a partial)

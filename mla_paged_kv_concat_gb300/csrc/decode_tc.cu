@@ -51,6 +51,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "kernels.cuh"
 #include "ptx.cuh"
 #include "tc.cuh"
@@ -459,7 +461,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             have_o && __shfl_sync(0xffffffffu, npv < ns && mbar_test(p_full, npv & 1), 0);
         if (pv_ready) {
           tc::fence_after_sync();
-          if (lane == 0) {
+          if (tc::elect_one()) {
             // A = P (TMEM, 16 tokens = 8 packed columns per step); B = V:
             // MN-major, 128-byte swizzle (N step = next 64-dim box, K step =
             // 8 tokens = 1024 B; 16 tokens per MMA = 2048 B = 128 in the
@@ -501,23 +503,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             __syncwarp();
           }
           tc::fence_after_sync();
-          if (lane == 0) {
+          if (tc::elect_one()) {
             // S = Q K^T: A = Q from TMEM (16 dims = 8 packed columns per
             // step), B = K tile, K-major with 128-byte swizzle.  The
             // descriptor's start-address field (bytes / 16) is advanced by
             // addition: one 64-dim box is CHUNK_BYTES / 16, one 16-dim step 2.
+            // The sequence is unrolled for each rank's chunk count.
             const uint64_t d0 =
                 tc::smem_desc(stage_base + st * STAGE_BYTES, 16, 1024, tc::kLayoutSw128);
-#pragma unroll 1
-            for (int c = 0; c < nch; ++c) {
+            auto issue_s = [&](auto nch_c) {
+              constexpr int NC = decltype(nch_c)::value;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const int ks = c * 4 + kk;
+              for (int ks = 0; ks < NC * 4; ++ks)
                 tc::mma_ts(tmem + S_COL, tmem + Q_COL + ks * 8,
-                           d0 + static_cast<uint64_t>(c * (CHUNK_BYTES >> 4) + kk * 2), idS,
-                           ks > 0 ? 1u : 0u);
-              }
-            }
+                           d0 + static_cast<uint64_t>((ks >> 2) * (CHUNK_BYTES >> 4) +
+                                                      (ks & 3) * 2),
+                           idS, ks > 0 ? 1u : 0u);
+            };
+            if (nch == 4)
+              issue_s(std::integral_constant<int, 4>());
+            else
+              issue_s(std::integral_constant<int, 5>());
             tc::commit(s_full);
           }
           __syncwarp();
@@ -926,15 +932,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 
 }  // namespace
 
-int tc_split_group(const DecodeParams& p, int sm_count) {
-  // Fuse consecutive splits into CTA pairs.  With f splits per pair the
-  // launch has units * ceil(S / f) pairs; the estimated cost (in units of one
-  // split's KV stream) is the number of waves times the work of one pair, plus
-  // the partial outputs each pair writes and the merge reads back (about 0.85
-  // of a split's bytes per 128-vector unit).  Pick f with the lowest cost.
+int tc_split_group(const DecodeParams& p, int sm_count, int ctas_per_unit) {
+  // Fuse consecutive splits into one CTA pair (ctas_per_unit 2) or CTA (1).
+  // With f splits per pair the launch has units * ceil(S / f) pairs; the
+  // estimated cost (in units of one split's KV stream) is the number of
+  // waves times the work of one pair, plus the partial outputs each pair
+  // writes and the merge reads back (about 0.85 of a split's bytes per
+  // 128-vector unit).  Pick f with the lowest cost.
   const int qblocks = (p.rows_per_seq * p.num_heads + 127) / 128;
   const int64_t units = static_cast<int64_t>(qblocks) * p.num_seqs;
-  const int64_t pairs = sm_count >= 2 ? sm_count / 2 : 1;
+  const int64_t pairs = sm_count >= ctas_per_unit ? sm_count / ctas_per_unit : 1;
   const int S = p.num_splits;
   int best_f = S;
   double best_cost = 1e300;

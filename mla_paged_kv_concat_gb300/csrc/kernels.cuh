@@ -134,8 +134,18 @@ cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap,
 // the previous kernel of the stream.
 cudaError_t launch_decode_tc(const DecodeParams& p, const CUtensorMap& tmap,
                              int split_group, int sm_count, cudaStream_t stream);
-// Consecutive splits the tcgen05 kernel processes per CTA pair.
-int tc_split_group(const DecodeParams& p, int sm_count);
+// Consecutive splits a tcgen05 kernel processes per unit of `ctas_per_unit`
+// CTAs (2: the 512-wide kernel's pairs; 1: the 256-wide kernel) in grid mode.
+int tc_split_group(const DecodeParams& p, int sm_count, int ctas_per_unit);
+
+// Stage 1 on tcgen05/TMEM for the 256-wide latent (R = 256), bf16 or fp8
+// cache, one CTA per 128 query vectors (no cluster).  With num_kv_splits > 1
+// (and at most kMaxPersistUnits (sequence, 128-vector block) units) it runs
+// persistent, one CTA per SM (`sm_count`); otherwise one CTA per 128 vectors
+// and group of `split_group` consecutive splits.  `tmap` as for the warp-MMA kernel.  Launched
+// overlapped with the previous kernel of the stream.
+cudaError_t launch_decode_tc1(const DecodeParams& p, const CUtensorMap& tmap, bool fp8,
+                              int split_group, int sm_count, cudaStream_t stream);
 
 // Stage 2: LSE merge of the split partials into o (bf16) and lse (fp32).
 // Every stage-1 kernel leaves, for each (row, head) of a non-empty sequence,

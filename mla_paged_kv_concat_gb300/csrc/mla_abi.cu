@@ -113,8 +113,9 @@ bool pow2_block(int bs) {
   return bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256;
 }
 
-// The tcgen05 kernel covers bf16 caches with a 512-wide latent.
-bool tc_supported(bool fp8, int R) { return !fp8 && R == 512; }
+// The tcgen05 kernels cover bf16 caches with a 512-wide latent (CTA pairs)
+// and bf16 or fp8 caches with a 256-wide latent (one CTA per 128 vectors).
+bool tc_supported(bool fp8, int R) { return R == 256 || (!fp8 && R == 512); }
 
 }  // namespace
 
@@ -398,14 +399,19 @@ mla_status prepare_decode(const void* q, int64_t q_row_stride,
   return MLA_OK;
 }
 
-// Stage-1 kernel choice: the tcgen05 kernel when forced, or (AUTO) when it
-// supports the cache and a sequence has at least 128 query vectors to fill
-// its M = 128 tile; the warp-MMA kernel otherwise.
+// Stage-1 kernel choice: a tcgen05 kernel when forced, or (AUTO) when one
+// supports the cache and the sequences have at least 64 query vectors for
+// its M = 128 tile; the warp-MMA kernel otherwise.  Measured on GB300
+// (32 sequences of 8192 tokens, stage 1 alone): the warp-MMA kernel's time
+// grows with the query vectors (its fragment loads from shared memory bound
+// it), the tcgen05 kernels' hardly; they tie near 32 vectors and the
+// tcgen05 kernels lead from 64 (R = 512 bf16: 128 against 143 us; R = 256:
+// 57 against 98 us bf16, 71 against 131 us E4M3) to 128 (2.0-3.3 x).
 bool use_tc(const mla::DecodeParams& p, bool fp8, int R, mla_decode_path path) {
   if (path == MLA_PATH_TCGEN05) return true;
   if (path == MLA_PATH_MMA_SYNC) return false;
-  return tc_supported(fp8, R) &&
-         static_cast<int64_t>(p.rows_per_seq) * p.num_heads >= 128;
+  const int64_t nvec = static_cast<int64_t>(p.rows_per_seq) * p.num_heads;
+  return tc_supported(fp8, R) && nvec >= 64;
 }
 
 // Everything stage 1 needs at launch time, computed once per call (or once
@@ -441,14 +447,19 @@ mla_status build_stage1(const mla::DecodeParams& p_in, const void* kv_cache, boo
                       ? 1
                       : 0;
   }
-  s1->split_group = s1->tc ? mla::tc_split_group(s1->p, s1->sm_count) : 1;
+  s1->split_group =
+      s1->tc ? mla::tc_split_group(s1->p, s1->sm_count, R == 256 ? 1 : 2) : 1;
   return MLA_OK;
 }
 
 mla_status launch_stage1(const Stage1& s1, cudaStream_t s) {
-  cudaError_t e = s1.tc ? mla::launch_decode_tc(s1.p, s1.tmap, s1.split_group, s1.sm_count, s)
-                        : mla::launch_decode_mma(s1.p, s1.tmap, s1.qmaps, s1.R, s1.fp8,
-                                                 s1.sm_count, s);
+  cudaError_t e;
+  if (!s1.tc)
+    e = mla::launch_decode_mma(s1.p, s1.tmap, s1.qmaps, s1.R, s1.fp8, s1.sm_count, s);
+  else if (s1.R == 256)
+    e = mla::launch_decode_tc1(s1.p, s1.tmap, s1.fp8, s1.split_group, s1.sm_count, s);
+  else
+    e = mla::launch_decode_tc(s1.p, s1.tmap, s1.split_group, s1.sm_count, s);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 

@@ -224,3 +224,42 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem,
 
 }  // namespace tc
 }  // namespace mla
+
+namespace mla {
+namespace tc {
+
+// D[tmem] (+)= A[smem] * B[smem], both operands by descriptor; issued by one
+// thread.
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+}  // namespace tc
+}  // namespace mla
+
+namespace mla {
+namespace tc {
+
+// One lane of a converged warp (elect.sync): the issuing lane of the
+// tcgen05.mma sequences.  Issuing from a warp-uniform region, with the
+// instruction sequence unrolled, keeps the operand descriptors in uniform
+// registers; measured on GB300, one issuing thread in a runtime loop took
+// 110-150 cycles per M=128 N=64 instruction, this form 42.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, e;\n\t}"
+      : "=r"(p));
+  return p != 0;
+}
+
+}  // namespace tc
+}  // namespace mla

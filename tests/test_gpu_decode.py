@@ -25,8 +25,9 @@ PATHS = [mla.MLA_PATH_MMA_SYNC, mla.MLA_PATH_TCGEN05]
 
 
 def tc_ok(w):
-    """The tcgen05 kernel covers bf16 caches with a 512-wide latent."""
-    return not w.kv_fp8 and w.kv_lora_rank == 512
+    """The tcgen05 kernels cover bf16 caches with a 512-wide latent and bf16
+    or fp8 caches with a 256-wide latent."""
+    return w.kv_lora_rank == 256 or not w.kv_fp8
 
 
 def _run(w, splits, path=mla.MLA_PATH_AUTO, pairs=None, write=True):
@@ -90,11 +91,16 @@ def test_full_head_deterministic_single_pass(cuda_dev):
     assert_close(o1, l1, o_ref, lse_ref, pairs=pairs, what="full_head S=1")
 
 
-def test_fp8_small(cuda_dev):
+@pytest.mark.parametrize("path", [mla.MLA_PATH_AUTO] + PATHS)
+def test_fp8_small(cuda_dev, path):
+    """B=32, H=32, E4M3 cache with R=256 at the benchmark's split count, on
+    both stage-1 kernels (AUTO takes the warp-MMA kernel below 64 query
+    vectors): the first and last vector of every (sequence, 32-vector) unit
+    (each sequence is one 128-vector unit of the tcgen05 schedule), plus
+    random pairs."""
     w = W.make("fp8_small")
     S = mla.mla_num_kv_splits(w.max_seq_len, sm_count())
-    # every (sequence, 32-vector) unit of the warp-MMA schedule, plus random pairs
-    _run(w, S, pairs=unit_pairs(w, 32, extra=64, seed=5))
+    _run(w, S, path, pairs=unit_pairs(w, 32, extra=64, seed=5))
 
 
 @pytest.mark.slow
@@ -138,15 +144,16 @@ SMALL = [
 def test_small_shapes(cuda_dev, case, splits, path):
     w = W.make_workload(f"small{case}", seed=200 + case, pool_blocks=None, **SMALL[case])
     if path == mla.MLA_PATH_TCGEN05 and not tc_ok(w):
-        pytest.skip("tcgen05 kernel: bf16 cache, R = 512 only")
+        pytest.skip("tcgen05 kernels: no fp8 cache with R = 512")
     _run(w, splits, path)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("splits", [1, 8])
 @pytest.mark.parametrize("q_exp,R,H,rows", [(20, 256, 32, 1), (-30, 512, 16, 1),
                                             (-100, 256, 16, 2), (None, 512, 32, 1),
                                             (None, 256, 128, 1)])
-def test_fp8_query_magnitudes(cuda_dev, q_exp, R, H, rows, splits):
+def test_fp8_query_magnitudes(cuda_dev, q_exp, R, H, rows, splits, path):
     """An fp8 cache against queries of extreme magnitude: every element times
     2^q_exp (far outside the fp8 and f16 ranges) with sm_scale times 2^-q_exp
     so that the scores stay moderate, or heads of different magnitudes
@@ -168,13 +175,19 @@ def test_fp8_query_magnitudes(cuda_dev, q_exp, R, H, rows, splits):
     w.q = q32.bfloat16()
     assert torch.equal(w.q.double(), q)  # power-of-two scaling is exact in bf16
     w.sm_scale = sm
-    _run(w, splits, mla.MLA_PATH_MMA_SYNC)
+    if path == mla.MLA_PATH_TCGEN05 and not tc_ok(w):
+        pytest.skip("tcgen05 kernels: no fp8 cache with R = 512")
+    _run(w, splits, path)
 
 
 @pytest.mark.parametrize("path", PATHS)
 def test_forced_kernel_rejects_what_it_does_not_cover(cuda_dev, path):
-    w = W.make_workload("rej", seed=64, seq_lens=[100], num_heads=16, kv_lora_rank=256)
+    """An fp8 cache with a 512-wide latent has no tcgen05 kernel: forcing one
+    is refused before any launch; the warp-MMA kernel covers it."""
+    w = W.make_workload("rej", seed=64, seq_lens=[100], num_heads=16, kv_fp8=True,
+                        kv_scale=0.05, write="all")
     d = Dev(w)
+    d.write()
     if path == mla.MLA_PATH_TCGEN05:
         with pytest.raises(mla.MlaError):
             d.decode(2, path=path)
@@ -257,13 +270,16 @@ def test_single_pass_is_batch_invariant(cuda_dev, path):
         assert torch.equal(o_b[0], o_all[b]) and torch.equal(l_b[0], l_all[b])
 
 
-@pytest.mark.parametrize("path", PATHS)
-def test_physical_block_permutation_is_bitwise_invariant(cuda_dev, path):
+@pytest.mark.parametrize("path,R,fp8", [(mla.MLA_PATH_MMA_SYNC, 512, False),
+                                         (mla.MLA_PATH_TCGEN05, 512, False),
+                                         (mla.MLA_PATH_TCGEN05, 256, True)])
+def test_physical_block_permutation_is_bitwise_invariant(cuda_dev, path, R, fp8):
     """Moving every block to another physical slot (and rewriting the table)
     leaves the output bit-for-bit unchanged (the paged-layout invariance of
     the pages' test_decode_attention, page size 1 vs 16)."""
+    kw = dict(kv_fp8=True, kv_scale=0.05, write="all") if fp8 else {}
     w = W.make_workload("perm", seed=61, seq_lens=[700, 129, 64], num_heads=16,
-                        pool_blocks=30)
+                        pool_blocks=30, kv_lora_rank=R, **kw)
     d = Dev(w)
     d.write()
     o1, l1 = [t.clone() for t in d.decode(4, path=path)]
@@ -271,7 +287,8 @@ def test_physical_block_permutation_is_bitwise_invariant(cuda_dev, path):
     new_cache = torch.empty_like(d.cache)
     new_cache[perm] = d.cache
     new_bt = perm[d.block_table.long()].int()
-    o2, l2 = mla.decode(d.q, new_cache, new_bt, d.seq_lens, w.sm_scale, 4, path=path)
+    o2, l2 = mla.decode(d.q, new_cache, new_bt, d.seq_lens, w.sm_scale, 4, path=path,
+                        kv_lora_rank=R, kv_scale=d.kv_scale if fp8 else None)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
