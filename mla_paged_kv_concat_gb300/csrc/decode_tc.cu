@@ -74,7 +74,8 @@ constexpr int XP_BYTES = XP_ALPHA + 64 * 4;
 constexpr int OFF_STAGE = 0;
 constexpr int OFF_XIN = OFF_STAGE + TSTAGES * STAGE_BYTES;  // peer partials, x2
 constexpr int OFF_PIN = OFF_XIN + 2 * XS_BYTES;             // P from the peer, x2
-constexpr int OFF_FIN = OFF_PIN + 2 * XP_BYTES;             // 1 / l from the peer
+constexpr int OFF_POUT = OFF_PIN + 2 * XP_BYTES;            // P for the peer (bulk-copied)
+constexpr int OFF_FIN = OFF_POUT + XP_BYTES;                // 1 / l from the peer
 constexpr int OFF_RED = OFF_FIN + 256;                      // own rows: max / sum exchange
 constexpr int OFF_PRE = OFF_RED + 6 * 64 * 4;               // schedule: unit tile prefix
 constexpr int OFF_LEN = OFF_PRE + (kMaxPersistUnits + 1) * 4;  // schedule: sequence lengths
@@ -567,6 +568,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     const float scale_log2 = p.sm_scale * kLog2e;
     const uint8_t* xin = smem + OFF_XIN;
     const uint8_t* pin = smem + OFF_PIN;
+    uint8_t* pout = smem + OFF_POUT;
     float* red = reinterpret_cast<float*>(smem + OFF_RED);  // [2 tiles][2 halves][64]
     float* lred = red + 2 * 2 * 64;                          // [2 halves][64]
     // The peer's buffers and barriers (messages are st.async stores that
@@ -792,6 +794,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           // other half reads this tile's value before either writes the
           // tile after next's)
           red[(bb * 2 + h) * 64 + xi] = mt;
+          // (the outbound P buffer is free once the previous tile's bulk copy
+          // has read it; its issuing thread checks before this barrier)
+          if (lead) tc::bulk_wait_read();
           if (!own_sync()) { ok = false; break; }
           mt = fmaxf(red[(bb * 2) * 64 + xi], red[(bb * 2 + 1) * 64 + xi]);
           // ---- online softmax with lazy rescaling (both halves take the
@@ -815,16 +820,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           l_run += (psum[0] + psum[1]) + (psum[2] + psum[3]);
           // ---- this half of P, and alpha, to the peer for its half of O
           // (its buffer bb held the P of tile n - 2, which it has stored: it
-          // sent this tile's partial scores only afterwards)
+          // sent this tile's partial scores only afterwards).  The 128 owner
+          // threads write their parts into the outbound buffer and one of
+          // them hands the 64 rows to the peer as one bulk copy, which runs
+          // in the background: per-thread remote stores stalled the owners
+          // behind the partial-score traffic in flight.
           {
-            const uint32_t dst = pin_peer + bb * XP_BYTES;
-            const uint32_t bar = pin_bar_peer0 + bb * 8;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              tc::st_async_v4u(dst + xoff(xi, 4 * h + j, XP_ROW), pk[4 * j], pk[4 * j + 1],
-                               pk[4 * j + 2], pk[4 * j + 3], bar);
-            if (h == 0) tc::st_async_b32(dst + XP_ALPHA + 4 * xi, __float_as_uint(alpha), bar);
+              *reinterpret_cast<uint4*>(pout + xoff(xi, 4 * h + j, XP_ROW)) =
+                  make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            if (h == 0) reinterpret_cast<float*>(pout + XP_ALPHA)[xi] = alpha;
+            fence_proxy_async_smem();  // the bulk copy reads through the async proxy
           }
+          if (!own_sync()) { ok = false; break; }
+          if (lead)
+            tc::bulk_copy_to_peer(pin_peer + bb * XP_BYTES, pout, XP_BYTES, pin_bar_peer0 + bb * 8);
           if (!rescale_o(n, n0, alpha)) { ok = false; break; }
           if (n >= 1 && !warp_wait(pv_done, (n - 1) & 1)) { ok = false; break; }
           tc::fence_after_sync();
@@ -837,6 +848,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           if (!own_sync()) ok = false;
           l_run = lred[xi] + lred[64 + xi];
         }
+        // the last copy has read the outbound buffer before this CTA can
+        // leave (the next segment's first tile waits for it anyway)
+        if (lead) tc::bulk_wait_read();
       }
 
       // ---- the owner's 1 / l reaches the other CTA as the segment's last

@@ -263,3 +263,26 @@ __device__ __forceinline__ bool elect_one() {
 
 }  // namespace tc
 }  // namespace mla
+
+namespace mla {
+namespace tc {
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory to a cluster peer's, completing the bytes
+// on the peer's mbarrier (cluster addresses from map_peer); one thread.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void* src,
+                                                  uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst_cluster),
+      "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until this thread's bulk copies have read their sources.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+}  // namespace tc
+}  // namespace mla
