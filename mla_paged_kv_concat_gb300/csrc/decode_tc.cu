@@ -62,7 +62,7 @@ namespace mla {
 namespace {
 
 constexpr int TBN = 64;                   // tokens per tile
-constexpr int TSTAGES = 4;                // KV ring depth
+constexpr int TSTAGES = 3;                // KV ring depth
 constexpr int TMAXCH = 5;                 // max 64-dim chunks per CTA
 constexpr int CHUNK_BYTES = TBN * 128;    // one 64-dim box of a tile (8 KiB)
 constexpr int STAGE_BYTES = TMAXCH * CHUNK_BYTES;
@@ -75,7 +75,8 @@ constexpr int OFF_STAGE = 0;
 constexpr int OFF_XIN = OFF_STAGE + TSTAGES * STAGE_BYTES;  // peer partials, x2
 constexpr int OFF_PIN = OFF_XIN + 2 * XS_BYTES;             // P from the peer, x2
 constexpr int OFF_POUT = OFF_PIN + 2 * XP_BYTES;            // P for the peer (bulk-copied)
-constexpr int OFF_FIN = OFF_POUT + XP_BYTES;                // 1 / l from the peer
+constexpr int OFF_XOUT = OFF_POUT + XP_BYTES;               // partials for the peer (bulk-copied)
+constexpr int OFF_FIN = OFF_XOUT + XS_BYTES;                // 1 / l from the peer
 constexpr int OFF_RED = OFF_FIN + 256;                      // own rows: max / sum exchange
 constexpr int OFF_PRE = OFF_RED + 6 * 64 * 4;               // schedule: unit tile prefix
 constexpr int OFF_LEN = OFF_PRE + (kMaxPersistUnits + 1) * 4;  // schedule: sequence lengths
@@ -569,6 +570,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     const uint8_t* xin = smem + OFF_XIN;
     const uint8_t* pin = smem + OFF_PIN;
     uint8_t* pout = smem + OFF_POUT;
+    uint8_t* xout = smem + OFF_XOUT;
     float* red = reinterpret_cast<float*>(smem + OFF_RED);  // [2 tiles][2 halves][64]
     float* lred = red + 2 * 2 * 64;                          // [2 halves][64]
     // The peer's buffers and barriers (messages are st.async stores that
@@ -736,12 +738,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             tc::reg_fence(sr);
             const int bb = ns & 1;
             if (lead) mbar_arrive_expect_tx(&pin_full[bb], XP_BYTES);  // P of tile ns
-            const uint32_t dst = xin_peer + bb * XS_BYTES;
-            const uint32_t bar = xin_bar_peer0 + bb * 8;
+            // The warp's 32 rows go to the peer as one bulk copy of a local
+            // copy (its previous copy has read that buffer first).
+            const uint32_t base = (xi & ~31u) * XS_ROW;
+            if (lane == 0) tc::bulk_wait_read();
+            __syncwarp();
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              tc::st_async_v4u(dst + xoff(xi, j, XS_ROW), sr[4 * j], sr[4 * j + 1],
-                               sr[4 * j + 2], sr[4 * j + 3], bar);
+              *reinterpret_cast<uint4*>(xout + xoff(xi, j, XS_ROW)) =
+                  make_uint4(sr[4 * j], sr[4 * j + 1], sr[4 * j + 2], sr[4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+              tc::bulk_copy_to_peer(xin_peer + bb * XS_BYTES + base, xout + base, 32 * XS_ROW,
+                                    xin_bar_peer0 + bb * 8);
             ++ns;
             did = true;
           }
@@ -758,6 +768,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             }
           }
         }
+        if (lane == 0) tc::bulk_wait_read();  // the local copy is read before leaving
       } else {
         for (int n = n0; n < n1 && ok; ++n) {
           const int bb = n & 1;              // exchange buffer
