@@ -51,7 +51,6 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include <type_traits>
 
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -62,10 +61,11 @@ namespace mla {
 namespace {
 
 constexpr int TBN = 64;                   // tokens per tile
-constexpr int TSTAGES = 3;                // KV ring depth
-constexpr int TMAXCH = 5;                 // max 64-dim chunks per CTA
+constexpr int TSTAGES = 4;                // KV ring depth
+constexpr int TLAT = 4;                   // 64-dim latent chunks per CTA
 constexpr int CHUNK_BYTES = TBN * 128;    // one 64-dim box of a tile (8 KiB)
-constexpr int STAGE_BYTES = TMAXCH * CHUNK_BYTES;
+constexpr int ROPE_BYTES = TBN * 64;      // the CTA's 32 rope dims of a tile
+constexpr int STAGE_BYTES = TLAT * CHUNK_BYTES + ROPE_BYTES;
 constexpr int XS_ROW = TBN * 4;           // bytes of one partial-score row
 constexpr int XS_BYTES = 64 * XS_ROW;     // 64 vectors' partial scores
 constexpr int XP_ROW = TBN * 2;           // bytes of one P row (bf16)
@@ -88,7 +88,7 @@ constexpr int TC_THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t S_COL = 256;  // S, 64 fp32 columns
 constexpr uint32_t P_COL = 320;  // P, 64 bf16 in 32 columns
-constexpr uint32_t Q_COL = 352;  // Q, up to 320 bf16 in 160 columns
+constexpr uint32_t Q_COL = 352;  // Q, 288 bf16 in 144 columns
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -131,7 +131,8 @@ constexpr int kClampedBit = 1 << 30;
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap,
-                     const int split_group, const int persistent) {
+                     const __grid_constant__ CUtensorMap rope_map, const int split_group,
+                     const int persistent) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -155,8 +156,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 
   const uint32_t rank = tc::cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
-  const int nch = rank == 0 ? 4 : 5;       // local 64-dim chunks
-  const int c0 = rank == 0 ? 0 : 4;        // first global chunk
+  // This CTA's dims of the 576: latent [256 rank, 256 rank + 256) as four
+  // 64-dim chunks and rope [32 rank, 32 rank + 32) (dims 512 + 32 rank on).
+  const int c0 = TLAT * rank;  // first latent chunk
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // The MMA issuer and the producer share the SM sub-partitions (warp % 4)
   // of the two softmax warps that only forward rows, not of the two that run
@@ -168,7 +170,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   const int qblocks = cdiv(nvec, 128);
   const int S = p.num_splits;
   const int Lmax = p.max_blocks * p.block_size;
-  if (threadIdx.x == 128) tma_prefetch_desc(&tmap);
+  if (threadIdx.x == 128) {
+    tma_prefetch_desc(&tmap);
+    tma_prefetch_desc(&rope_map);
+  }
   // Launched overlapped with the previous kernel of the stream: nothing in
   // global memory is read before it has completed.
   griddep_wait();
@@ -418,7 +423,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           }
           const int npages = pages_of(t);
           mbar_arrive_expect_tx(&kv_full[st],
-                                static_cast<uint32_t>(npages * nch * rows_box * 128));
+                                static_cast<uint32_t>(npages * rows_box * (TLAT * 128 + 64)));
           uint8_t* dst = smem + OFF_STAGE + st * STAGE_BYTES;
 #pragma unroll
           for (int pg = 0; pg < 4; ++pg) {
@@ -428,9 +433,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             const int row0 = tk % bs;
             if ((blk < 0 || blk >= p.num_blocks) && p.err_count && rank == 0)
               atomicAdd(p.err_count, 1);
-            for (int cl = 0; cl < nch; ++cl)
+            for (int cl = 0; cl < TLAT; ++cl)
               tma_load_3d(dst + cl * CHUNK_BYTES + pg * rows_box * 128, &tmap,
                           &kv_full[st], (c0 + cl) * 64, row0, blk);
+            tma_load_3d(dst + TLAT * CHUNK_BYTES + pg * rows_box * 64, &rope_map, &kv_full[st],
+                        512 + 32 * static_cast<int>(rank), row0, blk);
           }
 #pragma unroll
           for (int pg = 0; pg < 4; ++pg) cur[pg] = nxt[pg];
@@ -492,12 +499,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           const int st = ns % TSTAGES;
           const int valid = min(TBN, sg.end - (sg.start + (ns - n0) * TBN));
           if (valid < TBN) {
-            // Rows past the segment end hold other tokens or NaN: zero them
-            // so the P.V product sees 0 * 0 there (their scores are masked).
+            // Rows past the segment end hold other tokens or NaN: zero their
+            // latent part so the P.V product sees 0 * 0 there (their scores
+            // are masked; the rope part only enters those scores).
             uint8_t* stp = smem + OFF_STAGE + st * STAGE_BYTES;
-            const int nz = (TBN - valid) * nch * 8;
+            const int nz = (TBN - valid) * TLAT * 8;
             for (int i = lane; i < nz; i += 32) {
-              const int r = valid + i / (nch * 8), rem = i % (nch * 8);
+              const int r = valid + i / (TLAT * 8), rem = i % (TLAT * 8);
               *reinterpret_cast<uint4*>(stp + (rem >> 3) * CHUNK_BYTES + r * 128 +
                                         (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
             }
@@ -507,25 +515,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           tc::fence_after_sync();
           if (tc::elect_one()) {
             // S = Q K^T: A = Q from TMEM (16 dims = 8 packed columns per
-            // step), B = K tile, K-major with 128-byte swizzle.  The
-            // descriptor's start-address field (bytes / 16) is advanced by
-            // addition: one 64-dim box is CHUNK_BYTES / 16, one 16-dim step 2.
-            // The sequence is unrolled for each rank's chunk count.
-            const uint64_t d0 =
-                tc::smem_desc(stage_base + st * STAGE_BYTES, 16, 1024, tc::kLayoutSw128);
-            auto issue_s = [&](auto nch_c) {
-              constexpr int NC = decltype(nch_c)::value;
+            // step), B = K tile, K-major: the latent chunks with 128-byte
+            // swizzle (8-row groups 1024 B apart), then the rope part with
+            // 64-byte swizzle (groups 512 B apart).  The descriptor's
+            // start-address field (bytes / 16) is advanced by addition: one
+            // 64-dim box is CHUNK_BYTES / 16, one 16-dim step 2.
+            const uint32_t sa = stage_base + st * STAGE_BYTES;
+            const uint64_t d0 = tc::smem_desc(sa, 16, 1024, tc::kLayoutSw128);
+            const uint64_t dr = tc::smem_desc(sa + TLAT * CHUNK_BYTES, 16, 512, tc::kLayoutSw64);
 #pragma unroll
-              for (int ks = 0; ks < NC * 4; ++ks)
-                tc::mma_ts(tmem + S_COL, tmem + Q_COL + ks * 8,
-                           d0 + static_cast<uint64_t>((ks >> 2) * (CHUNK_BYTES >> 4) +
-                                                      (ks & 3) * 2),
-                           idS, ks > 0 ? 1u : 0u);
-            };
-            if (nch == 4)
-              issue_s(std::integral_constant<int, 4>());
-            else
-              issue_s(std::integral_constant<int, 5>());
+            for (int ks = 0; ks < TLAT * 4; ++ks)
+              tc::mma_ts(tmem + S_COL, tmem + Q_COL + ks * 8,
+                         d0 + static_cast<uint64_t>((ks >> 2) * (CHUNK_BYTES >> 4) + (ks & 3) * 2),
+                         idS, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kr = 0; kr < 2; ++kr)
+              tc::mma_ts(tmem + S_COL, tmem + Q_COL + TLAT * 32 + kr * 8,
+                         dr + static_cast<uint64_t>(kr * 2), idS, 1u);
             tc::commit(s_full);
           }
           __syncwarp();
@@ -624,9 +630,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       mbar_arrive(s_free);
     };
 
-    // ---- Q of a segment: this thread's vector, dims [64*c0, 64*(c0+nch)),
-    // into TMEM lane row_i as packed bf16 pairs (padding vectors are zeros);
-    // on own rows the two warps take half of the chunks each.  Called once
+    // ---- Q of a segment: this thread's vector, the CTA's latent dims (four
+    // 64-dim chunks) and then its 32 rope dims, into TMEM lane row_i as
+    // packed bf16 pairs (padding vectors are zeros); on own rows one warp
+    // takes chunks 0-1, the other chunks 2-3 and the rope part.  Called once
     // the previous segment's S products, which read Q, are complete (this
     // thread has loaded all of them).
     auto load_q = [&](const TcSeg& sg) {
@@ -634,17 +641,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       const bool valid_v = v < nvec;
       const int row = valid_v ? sg.b * p.rows_per_seq + v / H : 0;
       const int hd = valid_v ? v % H : 0;
-      const int half = (nch + 1) / 2;
-      const int q_lo = own ? h * half : 0, q_hi = own ? (h ? nch : half) : nch;
+      const int q_lo = own ? 2 * h : 0, q_hi = own ? 2 * h + 2 : TLAT;
+      const bool q_rope = !own || h == 1;
       // dims [0, 512) come from q_nope, [512, 576) from q_pe
       const uint16_t* qn = valid_v ? p.q + row * p.q_row_stride + hd * p.q_head_stride : p.q;
       const uint16_t* qp =
           valid_v ? p.q_pe + row * p.q_pe_row_stride + hd * p.q_pe_head_stride : p.q_pe;
       uint32_t r[2][32];
       auto load_chunk = [&](int c, uint32_t (&d)[32]) {
-        const int gc = c0 + c;  // 64-dim chunk of the 576-dim vector
-        const uint4* src =
-            reinterpret_cast<const uint4*>(gc < 8 ? qn + gc * 64 : qp + (gc - 8) * 64);
+        const uint4* src = reinterpret_cast<const uint4*>(qn + (c0 + c) * 64);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint4 x = valid_v ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
@@ -665,6 +670,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           tc::st_32x32b_x32(tmem + lane_base + Q_COL + (c + 1) * 32, r[1]);
         }
       }
+      if (q_rope) {
+        const uint4* src = reinterpret_cast<const uint4*>(qp + 32 * rank);
+        uint32_t d[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 x = valid_v ? __ldg(src + j) : make_uint4(0, 0, 0, 0);
+          d[4 * j] = x.x;
+          d[4 * j + 1] = x.y;
+          d[4 * j + 2] = x.z;
+          d[4 * j + 3] = x.w;
+        }
+        tc::st_32x32b_x16(tmem + lane_base + Q_COL + TLAT * 32, d);
+      }
       tc::wait_st();
       tc::fence_before_sync();
       mbar_arrive(q_ready);
@@ -676,10 +694,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       const int row = sg.b * p.rows_per_seq + v / H, hd = v % H;
       const uint16_t* qn = p.q + row * p.q_row_stride + hd * p.q_head_stride;
       const uint16_t* qp = p.q_pe + row * p.q_pe_row_stride + hd * p.q_pe_head_stride;
-      for (int c = 0; c < nch; ++c) {
-        const int gc = c0 + c;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(gc < 8 ? qn + gc * 64 : qp + (gc - 8) * 64));
-      }
+      for (int c = 0; c < TLAT; ++c)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + (c0 + c) * 64));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(qp + 32 * rank));
     };
 
     for_each_seg([&](const TcSeg& sg, int k, int n0, const TcSeg* next) -> bool {
@@ -985,7 +1002,8 @@ int tc_split_group(const DecodeParams& p, int sm_count, int ctas_per_unit) {
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, const CUtensorMap& tmap,
-                             int split_group, int sm_count, cudaStream_t stream) {
+                             const CUtensorMap& rope_map, int split_group, int sm_count,
+                             cudaStream_t stream) {
   static std::atomic<uint64_t> attr_done{0};  // one bit per device
   cudaError_t e = set_smem_attr_once(decode_tc_kernel, TC_SMEM, attr_done);
   if (e != cudaSuccess) return e;
@@ -995,12 +1013,12 @@ cudaError_t launch_decode_tc(const DecodeParams& p, const CUtensorMap& tmap,
     // persistent: one CTA pair per two SMs, tiles balanced over the pairs
     const int pairs = sm_count >= 2 ? sm_count / 2 : 1;
     return launch_overlapped(decode_tc_kernel, dim3(2 * pairs), dim3(TC_THREADS), TC_SMEM,
-                             stream, p, tmap, split_group, 1);
+                             stream, p, tmap, rope_map, split_group, 1);
   }
   const int groups = (p.num_splits + split_group - 1) / split_group;
   const dim3 grid(2 * qblocks, groups, p.num_seqs);
   return launch_overlapped(decode_tc_kernel, grid, dim3(TC_THREADS), TC_SMEM, stream, p, tmap,
-                           split_group, 0);
+                           rope_map, split_group, 0);
 }
 
 }  // namespace mla

@@ -130,10 +130,13 @@ cudaError_t launch_decode_mma(const DecodeParams& p, const CUtensorMap& tmap,
 // (sequence, 128-vector block) units) it runs persistent, sm_count / 2 pairs
 // with the tiles balanced over them; otherwise one pair per 128 vectors and
 // group of `split_group` consecutive splits.  `tmap` as above ({64,
-// min(block_size, 64), 1} box, 128-byte swizzle).  Launched overlapped with
-// the previous kernel of the stream.
+// min(block_size, 64), 1} box, 128-byte swizzle); `rope_map` the same tensor
+// with a {32, min(block_size, 64), 1} box and 64-byte swizzle (each CTA of a
+// pair takes half of the 64 rope dims).  Launched overlapped with the previous
+// kernel of the stream.
 cudaError_t launch_decode_tc(const DecodeParams& p, const CUtensorMap& tmap,
-                             int split_group, int sm_count, cudaStream_t stream);
+                             const CUtensorMap& rope_map, int split_group, int sm_count,
+                             cudaStream_t stream);
 // Consecutive splits a tcgen05 kernel processes per unit of `ctas_per_unit`
 // CTAs (2: the 512-wide kernel's pairs; 1: the 256-wide kernel) in grid mode.
 int tc_split_group(const DecodeParams& p, int sm_count, int ctas_per_unit);

@@ -53,7 +53,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // fp8 boxes land unswizzled, 64 bytes per row.
 mla_status make_cache_tmap(CUtensorMap* map, const void* cache, bool fp8,
                            int D, int block_size, int num_blocks,
-                           int64_t block_stride, int max_box_rows) {
+                           int64_t block_stride, int max_box_rows, int box_dims = 64) {
   auto fn = encode_fn();
   if (!fn) {
     snprintf(g_last_cuda_error, sizeof g_last_cuda_error,
@@ -67,15 +67,19 @@ mla_status make_cache_tmap(CUtensorMap* map, const void* cache, bool fp8,
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * elt,
                            static_cast<cuuint64_t>(block_stride) * elt};
   cuuint32_t box[3] = {
-      64, static_cast<cuuint32_t>(block_size < max_box_rows ? block_size : max_box_rows), 1};
+      static_cast<cuuint32_t>(box_dims),
+      static_cast<cuuint32_t>(block_size < max_box_rows ? block_size : max_box_rows), 1};
+  // a bf16 box 32 dims wide (64-byte rows) lands with the 64-byte swizzle
+  const CUtensorMapSwizzle swz = fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                 : box_dims == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                  : CU_TENSOR_MAP_SWIZZLE_128B;
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map,
                   fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                   3, const_cast<void*>(cache), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     snprintf(g_last_cuda_error, sizeof g_last_cuda_error,
@@ -419,6 +423,7 @@ bool use_tc(const mla::DecodeParams& p, bool fp8, int R, mla_decode_path path) {
 struct Stage1 {
   mla::DecodeParams p;
   CUtensorMap tmap;
+  CUtensorMap rope_map;  // the 512-wide tcgen05 kernel's 32-dim rope boxes
   mla::QMaps qmaps;
   bool tc, fp8;
   int R, split_group, sm_count;
@@ -436,6 +441,12 @@ mla_status build_stage1(const mla::DecodeParams& p_in, const void* kv_cache, boo
   mla_status st = make_cache_tmap(&s1->tmap, kv_cache, fp8, R + 64, block_size, num_blocks,
                                   block_stride, 64);
   if (st != MLA_OK) return st;
+  memset(&s1->rope_map, 0, sizeof s1->rope_map);
+  if (s1->tc && R == 512) {
+    st = make_cache_tmap(&s1->rope_map, kv_cache, fp8, R + 64, block_size, num_blocks,
+                         block_stride, 64, 32);
+    if (st != MLA_OK) return st;
+  }
   memset(&s1->qmaps, 0, sizeof s1->qmaps);
   s1->p.q_tma = 0;
   if (!s1->tc) {
@@ -459,7 +470,7 @@ mla_status launch_stage1(const Stage1& s1, cudaStream_t s) {
   else if (s1.R == 256)
     e = mla::launch_decode_tc1(s1.p, s1.tmap, s1.fp8, s1.split_group, s1.sm_count, s);
   else
-    e = mla::launch_decode_tc(s1.p, s1.tmap, s1.split_group, s1.sm_count, s);
+    e = mla::launch_decode_tc(s1.p, s1.tmap, s1.rope_map, s1.split_group, s1.sm_count, s);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e);
 }
 

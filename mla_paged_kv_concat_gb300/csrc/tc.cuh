@@ -40,7 +40,7 @@ __device__ __forceinline__ void fence_after_sync() {
 // ------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor: start address, leading- and stride-
 // dimension byte offsets (all >> 4), descriptor version 1, layout type in the
-// top three bits (0 = no swizzle, 2 = 128-byte swizzle).
+// top three bits (0 = no swizzle, 2 = 128-byte, 4 = 64-byte swizzle).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo,
                                               uint32_t sbo, uint32_t layout) {
   uint64_t d = 0;
@@ -53,6 +53,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo,
 }
 constexpr uint32_t kLayoutNone = 0;
 constexpr uint32_t kLayoutSw128 = 2;
+constexpr uint32_t kLayoutSw64 = 4;
 
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulation.
 // a_mn / b_mn: operand stored MN-major (1) or K-major (0).
