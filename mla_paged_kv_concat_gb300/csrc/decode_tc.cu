@@ -81,7 +81,7 @@ constexpr int OFF_RED = OFF_FIN + 256;                      // own rows: max / s
 constexpr int OFF_PRE = OFF_RED + 6 * 64 * 4;               // schedule: unit tile prefix
 constexpr int OFF_LEN = OFF_PRE + (kMaxPersistUnits + 1) * 4;  // schedule: sequence lengths
 constexpr int OFF_BAR = (OFF_LEN + kMaxPersistUnits * 4 + 7) & ~7;
-constexpr int NBARS = 2 * TSTAGES + 5 + 8;
+constexpr int NBARS = 2 * TSTAGES + 5 + 7;
 constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
 constexpr int TC_SMEM = OFF_TMEMSLOT + 16 + 1024;  // + alignment slack
 constexpr int TC_THREADS = 256;
@@ -149,7 +149,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   uint64_t* fin_full = s_full + 9;   // peer's 1 / l landed (one per segment)
   uint64_t* q_ready = s_full + 10;   // Q of the segment is in TMEM
   uint64_t* o_free = s_full + 11;    // the segment's O has been read out
-  uint64_t* own_bar = s_full + 12;   // the four warps of this CTA's own rows
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEMSLOT);
   int* pre = reinterpret_cast<int*>(smem + OFF_PRE);
   int* lens = reinterpret_cast<int*>(smem + OFF_LEN);
@@ -370,7 +369,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     mbar_init(fin_full, 1);
     mbar_init(q_ready, 192);
     mbar_init(o_free, 192);
-    mbar_init(own_bar, 128);
     fence_mbar_init();
   }
   if (warp == mma_warp) {
@@ -588,14 +586,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     const uint32_t pin_bar_peer0 = tc::map_peer(smem_u32(&pin_full[0]), peer);
     const uint32_t fin_bar_peer = tc::map_peer(smem_u32(fin_full), peer);
     bool ok = true;
-    uint32_t own_phase = 0;
-    // Barrier of the four warps of this CTA's own rows (bounded wait).
-    auto own_sync = [&]() -> bool {
-      mbar_arrive(own_bar);
-      const bool r = warp_wait(own_bar, own_phase & 1);
-      ++own_phase;
-      return r;
-    };
+    // Meeting of the four warps of this CTA's own rows (named barrier 1),
+    // which also ANDs their flags.  Every wait of theirs is bounded, so each
+    // reaches every meeting; one that gave up on a wait passes false, and
+    // all four take the same exit after the meeting.
+    auto own_sync = [&](bool good) -> bool { return named_bar_and(1, 128, good); };
     // This thread's O columns: all 256 on forwarding rows, half on own rows.
     const int o_c0 = own ? 128 * h : 0, o_c1 = own ? 128 * h + 128 : 256;
 
@@ -787,36 +782,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         }
         if (lane == 0) tc::bulk_wait_read();  // the local copy is read before leaving
       } else {
-        for (int n = n0; n < n1 && ok; ++n) {
+        bool bad = false;  // this warp gave up on a wait since the last meeting
+        for (int n = n0; n < n1; ++n) {
           const int bb = n & 1;              // exchange buffer
           const uint32_t u = (n >> 1) & 1;   // its phase parity
-          // ---- this half's 32 partial scores
-          if (!warp_wait(s_full, n & 1)) { ok = false; break; }
-          tc::fence_after_sync();
           uint32_t sr[32];
-          tc::ld_32x32b_x32(tmem + lane_base + S_COL + 32 * h, sr);
-          s_done();
-          tc::reg_fence(sr);
-          // ---- add the peer's partial scores for them (xin[bb] is not
-          // rewritten before the peer has received this tile's P)
-          if (lead) mbar_arrive_expect_tx(&xin_full[bb], XS_BYTES);
-          if (!warp_wait_cluster(&xin_full[bb], u)) { ok = false; break; }
-          const uint8_t* src = xin + bb * XS_BYTES;
-          const int valid = min(TBN, sg.end - (sg.start + (n - n0) * TBN)) - 32 * h;
           float mt = -INFINITY;
+          // ---- this half's 32 partial scores
+          if (!bad && warp_wait(s_full, n & 1)) {
+            tc::fence_after_sync();
+            tc::ld_32x32b_x32(tmem + lane_base + S_COL + 32 * h, sr);
+            s_done();
+            tc::reg_fence(sr);
+            // ---- add the peer's partial scores for them (xin[bb] is not
+            // rewritten before the peer has received this tile's P)
+            if (lead) mbar_arrive_expect_tx(&xin_full[bb], XS_BYTES);
+            if (warp_wait_cluster(&xin_full[bb], u)) {
+              const uint8_t* src = xin + bb * XS_BYTES;
+              const int valid = min(TBN, sg.end - (sg.start + (n - n0) * TBN)) - 32 * h;
 #pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            const float4 t =
-                *reinterpret_cast<const float4*>(src + xoff(xi, 8 * h + j4, XS_ROW));
-            const float tv[4] = {t.x, t.y, t.z, t.w};
+              for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 t =
+                    *reinterpret_cast<const float4*>(src + xoff(xi, 8 * h + j4, XS_ROW));
+                const float tv[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 4 * j4 + e;
-              const float s = __uint_as_float(sr[j]) + tv[e];
-              const float x = j < valid ? s * scale_log2 : -INFINITY;
-              sr[j] = __float_as_uint(x);
-              mt = fmaxf(mt, x);
+                for (int e = 0; e < 4; ++e) {
+                  const int j = 4 * j4 + e;
+                  const float s = __uint_as_float(sr[j]) + tv[e];
+                  const float x = j < valid ? s * scale_log2 : -INFINITY;
+                  sr[j] = __float_as_uint(x);
+                  mt = fmaxf(mt, x);
+                }
+              }
+            } else {
+              bad = true;
             }
+          } else {
+            bad = true;
           }
           // ---- row maximum over both halves (buffer by tile parity: the
           // other half reads this tile's value before either writes the
@@ -825,7 +827,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           // (the outbound P buffer is free once the previous tile's bulk copy
           // has read it; its issuing thread checks before this barrier)
           if (lead) tc::bulk_wait_read();
-          if (!own_sync()) { ok = false; break; }
+          if (!own_sync(!bad)) { ok = false; break; }
           mt = fmaxf(red[(bb * 2) * 64 + xi], red[(bb * 2 + 1) * 64 + xi]);
           // ---- online softmax with lazy rescaling (both halves take the
           // same decision from the same values)
@@ -861,19 +863,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             if (h == 0) reinterpret_cast<float*>(pout + XP_ALPHA)[xi] = alpha;
             fence_proxy_async_smem();  // the bulk copy reads through the async proxy
           }
-          if (!own_sync()) { ok = false; break; }
+          own_sync(true);  // (no wait since the last meeting)
           if (lead)
             tc::bulk_copy_to_peer(pin_peer + bb * XP_BYTES, pout, XP_BYTES, pin_bar_peer0 + bb * 8);
-          if (!rescale_o(n, n0, alpha)) { ok = false; break; }
-          if (n >= 1 && !warp_wait(pv_done, (n - 1) & 1)) { ok = false; break; }
+          if (!rescale_o(n, n0, alpha) || (n >= 1 && !warp_wait(pv_done, (n - 1) & 1))) {
+            bad = true;  // the next meeting ends the loop
+            continue;
+          }
           tc::fence_after_sync();
           tc::st_32x32b_x16(tmem + lane_base + P_COL + 16 * h, pk);
           p_ready();
         }
-        // ---- row sum over both halves
+        // ---- row sum over both halves (all four warps leave the loop
+        // together, so all four come here; a failure in the last tile's
+        // second half shows at this meeting)
         if (ok) {
           lred[h * 64 + xi] = l_run;
-          if (!own_sync()) ok = false;
+          if (!own_sync(!bad)) ok = false;
           l_run = lred[xi] + lred[64 + xi];
         }
         // the last copy has read the outbound buffer before this CTA can
@@ -903,7 +909,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       if (next) load_q(*next);
       // ---- epilogue: this thread's O columns (normalised) and, from the
       // owner, lse
-      if (!warp_wait(pv_done, (n1 - 1) & 1)) { ok = false; return false; }
+      const bool pv_ok = warp_wait(pv_done, (n1 - 1) & 1);
+      if ((own && !own_sync(pv_ok)) || !pv_ok) {  // the owners leave together
+        ok = false;
+        return false;
+      }
       tc::fence_after_sync();
       const int64_t rec = (static_cast<int64_t>(row) * S + sg.slot) * H + hd;
       // two TMEM loads in flight: columns c + 32 come in while c is stored
