@@ -51,6 +51,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -755,10 +757,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             const uint32_t base = (xi & ~31u) * XS_ROW;
             if (lane == 0) tc::bulk_wait_read();
             __syncwarp();
+            // (sent scaled by sm_scale * log2(e): the owner's sum is then
+            // one fused multiply-add)
+            auto scaled = [&](int k) {
+              return __float_as_uint(__uint_as_float(sr[k]) * scale_log2);
+            };
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               *reinterpret_cast<uint4*>(xout + xoff(xi, j, XS_ROW)) =
-                  make_uint4(sr[4 * j], sr[4 * j + 1], sr[4 * j + 2], sr[4 * j + 3]);
+                  make_uint4(scaled(4 * j), scaled(4 * j + 1), scaled(4 * j + 2),
+                             scaled(4 * j + 3));
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
@@ -800,20 +808,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             if (warp_wait_cluster(&xin_full[bb], u)) {
               const uint8_t* src = xin + bb * XS_BYTES;
               const int valid = min(TBN, sg.end - (sg.start + (n - n0) * TBN)) - 32 * h;
+              // x = (own partial + peer partial) * sm_scale * log2(e), the
+              // peer's part arriving scaled; tokens past the segment end
+              // (only in its last tile) get -inf
+              auto add_partials = [&](auto masked) {
 #pragma unroll
-              for (int j4 = 0; j4 < 8; ++j4) {
-                const float4 t =
-                    *reinterpret_cast<const float4*>(src + xoff(xi, 8 * h + j4, XS_ROW));
-                const float tv[4] = {t.x, t.y, t.z, t.w};
+                for (int j4 = 0; j4 < 8; ++j4) {
+                  const float4 t =
+                      *reinterpret_cast<const float4*>(src + xoff(xi, 8 * h + j4, XS_ROW));
+                  const float tv[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int j = 4 * j4 + e;
-                  const float s = __uint_as_float(sr[j]) + tv[e];
-                  const float x = j < valid ? s * scale_log2 : -INFINITY;
-                  sr[j] = __float_as_uint(x);
-                  mt = fmaxf(mt, x);
+                  for (int e = 0; e < 4; ++e) {
+                    const int j = 4 * j4 + e;
+                    float x = fmaf(__uint_as_float(sr[j]), scale_log2, tv[e]);
+                    if (decltype(masked)::value) x = j < valid ? x : -INFINITY;
+                    sr[j] = __float_as_uint(x);
+                    mt = fmaxf(mt, x);
+                  }
                 }
-              }
+              };
+              if (valid >= 32)
+                add_partials(std::false_type());
+              else
+                add_partials(std::true_type());
             } else {
               bad = true;
             }
