@@ -11,36 +11,38 @@
 // one sequence) share every KV row, so the work is a dense contraction:
 // S = Q K^T (M=128 vectors, N=64 tokens, K=576) and O = P V (M=128, N=512,
 // K=64).  An fp32 O of 128 x 512 fills all of a CTA's TMEM (512 columns), so
-// the latent dimension is split over a 2-CTA cluster:
-//   rank 0 holds dims [0, 256)   : S partial over them, O[:, 0:256)
-//   rank 1 holds dims [256, 576) : S partial over them, O[:, 256:512)
+// the work is split over a 2-CTA cluster by dims:
+//   rank r holds latent dims [256 r, 256 r + 256) and rope dims
+//   [32 r, 32 r + 32): its S partial over them, and O[:, 256 r : 256 r + 256)
 // Each CTA loads only its own dims of every KV tile (no byte is read twice)
 // and computes its partial S into TMEM.  The softmax of vector v is owned by
 // one CTA (rank v / 64): the other CTA sends it its partial S row for v
-// (fp32, one bulk shared-memory copy per tile for 64 vectors), the owner adds
-// the two partials, runs the online softmax and sends P (bf16) back with the
-// row's rescale factor; both CTAs then accumulate their half of O with P as
-// the A operand.  Per tile and direction that is 16 KiB of scores plus 8 KiB
-// of P, and each CTA evaluates only 64 x 64 exponentials.
+// (fp32, bulk shared-memory copies per 32-token half), the owner adds the
+// two partials, runs the online softmax and writes its P rows (bf16) into
+// the P buffer of both CTAs (its own, and the peer's by a bulk copy, with
+// the rows' rescale factors); both CTAs then accumulate their half of O with
+// that buffer as the A operand.  Per tile and direction that is 16 KiB of
+// scores plus 8 KiB of P, and each CTA evaluates only 64 x 64 exponentials.
 //
-// TMEM (512 columns): O [0, 256), S [256, 320), P [320, 352) as packed
-// bf16, Q [352, 512) as packed bf16 (rank 1 needs 160 columns for its 320
-// dims).  Q and P are A operands read straight from TMEM by the MMAs; only K
-// and V tiles (a 4-stage ring of 64 tokens) and the exchange buffers live in
-// shared memory.
+// TMEM (512 columns): O [0, 256); S [256, 352) as a ring of three 32-token
+// slots (S is computed per 32-token half, so the next tile's first half can
+// be computed before this tile's S has been read); Q [352, 496) as packed
+// bf16.  Q is an A operand read from TMEM; K and V tiles (a 4-stage ring of
+// 64 tokens), the P buffers (two, by tile parity) and the exchange buffers
+// live in shared memory.
 //
 // Roles per CTA (256 threads):
 //   softmax: thread = TMEM lane = query vector.  The 64 vectors the peer
 //              owns are forwarded by the two warps of their lane quarters
-//              (partial scores out, P and the rescale factor in, whichever
-//              is ready); the 64 this CTA owns get four warps, two per lane
-//              quarter, each taking one half of the 64 tokens, which share
-//              the row maximum and sum through shared memory (lazy
-//              rescaling of O only when the running max grows by more than
-//              2^8);
-//   one warp   MMA issuer (one thread) and TMEM owner;
+//              (partial scores out, the rescale factors of returned P in,
+//              whichever is ready); the 64 this CTA owns get four warps,
+//              two per lane quarter, each taking one half of the 64 tokens,
+//              which share the row maximum and sum through shared memory
+//              (lazy rescaling of O only when the running max grows by more
+//              than 2^8);
+//   one warp   MMA issuer (one elected thread) and TMEM owner;
 //   one warp   TMA producer: 64-token tiles of the paged cache into a
-//              4-stage mbarrier ring (128-byte swizzled boxes).
+//              4-stage mbarrier ring (swizzled boxes).
 //   The MMA and producer warps sit on the lane quarters (sub-partitions) of
 //   the forwarding warps, the lighter softmax work.
 //
@@ -68,34 +70,38 @@ constexpr int TLAT = 4;                   // 64-dim latent chunks per CTA
 constexpr int CHUNK_BYTES = TBN * 128;    // one 64-dim box of a tile (8 KiB)
 constexpr int ROPE_BYTES = TBN * 64;      // the CTA's 32 rope dims of a tile
 constexpr int STAGE_BYTES = TLAT * CHUNK_BYTES + ROPE_BYTES;
-constexpr int XS_ROW = TBN * 4;           // bytes of one partial-score row
-constexpr int XS_BYTES = 64 * XS_ROW;     // 64 vectors' partial scores
-constexpr int XP_ROW = TBN * 2;           // bytes of one P row (bf16)
-constexpr int XP_ALPHA = 64 * XP_ROW;     // offset of the 64 per-row factors
-constexpr int XP_BYTES = XP_ALPHA + 64 * 4;
+// Partial scores travel as two planes, one per 32-token half, each 64 rows
+// of 128 bytes (the plane an own-row warp reads).
+constexpr int XS_PLANE = 64 * 128;
+constexpr int XS_BYTES = 2 * XS_PLANE;    // 64 vectors' partial scores of a tile
+// P of a tile, the A operand of P.V: 128 rows (vectors) of 64 bf16 tokens,
+// 128 bytes each, 128-byte swizzle; rows [64 r, 64 r + 64) are rank r's.
+constexpr int P_BYTES = 128 * 128;
+constexpr int P_HALF = 64 * 128;
 constexpr int OFF_STAGE = 0;
 constexpr int OFF_XIN = OFF_STAGE + TSTAGES * STAGE_BYTES;  // peer partials, x2
-constexpr int OFF_PIN = OFF_XIN + 2 * XS_BYTES;             // P from the peer, x2
-constexpr int OFF_POUT = OFF_PIN + 2 * XP_BYTES;            // P for the peer (bulk-copied)
-constexpr int OFF_XOUT = OFF_POUT + XP_BYTES;               // partials for the peer (bulk-copied)
-constexpr int OFF_FIN = OFF_XOUT + XS_BYTES;                // 1 / l from the peer
+constexpr int OFF_P = OFF_XIN + 2 * XS_BYTES;               // P, x2 (own half + peer's)
+constexpr int OFF_XOUT = OFF_P + 2 * P_BYTES;               // one plane per forwarding warp
+constexpr int OFF_AIN = OFF_XOUT + 2 * (XS_PLANE / 2);      // peer's rescale factors, x2
+constexpr int OFF_AOUT = OFF_AIN + 2 * 256;                 // own rescale factors
+constexpr int OFF_FIN = OFF_AOUT + 256;                     // 1 / l from the peer
 constexpr int OFF_RED = OFF_FIN + 256;                      // own rows: max / sum exchange
 constexpr int OFF_PRE = OFF_RED + 6 * 64 * 4;               // schedule: unit tile prefix
 constexpr int OFF_LEN = OFF_PRE + (kMaxPersistUnits + 1) * 4;  // schedule: sequence lengths
 constexpr int OFF_BAR = (OFF_LEN + kMaxPersistUnits * 4 + 7) & ~7;
-constexpr int NBARS = 2 * TSTAGES + 5 + 7;
+constexpr int NBARS = 2 * TSTAGES + 20;
 constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
 constexpr int TC_SMEM = OFF_TMEMSLOT + 16 + 1024;  // + alignment slack
 constexpr int TC_THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL = 256;  // S, 64 fp32 columns
-constexpr uint32_t P_COL = 320;  // P, 64 bf16 in 32 columns
+constexpr uint32_t S_COL = 256;  // S, a ring of three 32-token fp32 slots (96 columns)
 constexpr uint32_t Q_COL = 352;  // Q, 288 bf16 in 144 columns
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-static_assert(OFF_XIN % 1024 == 0 && XS_BYTES % 16 == 0 && XP_BYTES % 16 == 0,
+static_assert(OFF_XIN % 1024 == 0 && OFF_P % 1024 == 0 && OFF_XOUT % 16 == 0 &&
+                  OFF_AIN % 16 == 0 && OFF_AOUT % 16 == 0,
               "alignment");
 static_assert(TC_SMEM <= 227 * 1024, "shared memory");
 
@@ -141,16 +147,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = bars + TSTAGES;
-  uint64_t* s_full = bars + 2 * TSTAGES;
-  uint64_t* s_free = s_full + 1;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* pv_done = s_full + 3;
-  uint64_t* mma_done = s_full + 4;
-  uint64_t* xin_full = s_full + 5;   // [2] peer partial scores landed
-  uint64_t* pin_full = s_full + 7;   // [2] peer P landed
-  uint64_t* fin_full = s_full + 9;   // peer's 1 / l landed (one per segment)
-  uint64_t* q_ready = s_full + 10;   // Q of the segment is in TMEM
-  uint64_t* o_free = s_full + 11;    // the segment's O has been read out
+  // S is computed in halves of 32 tokens; half e of tile t is ring position
+  // q = 2 t + e, in TMEM slot q % 3, the (q / 3)-th use of that slot.
+  uint64_t* s_slot_full = bars + 2 * TSTAGES;  // [3] S half landed in the slot
+  uint64_t* s_slot_free = s_slot_full + 3;     // [3] the slot has been read
+  uint64_t* p_full = s_slot_free + 3;   // [2] P.V inputs of tiles with this parity ready
+  uint64_t* pv_done = p_full + 2;       // [2] P.V of tiles with this parity completed
+  uint64_t* mma_done = pv_done + 2;
+  uint64_t* xin_full = mma_done + 1;    // [2] peer partial scores landed
+  uint64_t* pin_full = xin_full + 2;    // [2] peer P landed
+  uint64_t* fin_full = pin_full + 2;    // peer's 1 / l landed (one per segment)
+  uint64_t* q_ready = fin_full + 1;     // Q of the segment is in TMEM
+  uint64_t* o_free = q_ready + 1;       // the segment's O has been read out
+  uint64_t* peer_pv = o_free + 1;       // [2] the peer's P.V of tiles with this parity completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEMSLOT);
   int* pre = reinterpret_cast<int*>(smem + OFF_PRE);
   int* lens = reinterpret_cast<int*>(smem + OFF_LEN);
@@ -358,11 +367,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    mbar_init(s_full, 1);
-    // S / P / Q / O hand-offs: 64 forwarding + 128 own-row threads
-    mbar_init(s_free, 192);
-    mbar_init(p_full, 192);
-    mbar_init(pv_done, 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&s_slot_full[i], 1);
+      // an S half is read by the 64 forwarding threads and the 64 own-row
+      // threads of its token half
+      mbar_init(&s_slot_free[i], 128);
+    }
+    // Q / O hand-offs: 64 forwarding + 128 own-row threads; P: the six
+    // softmax warps
+    mbar_init(&p_full[0], 6);
+    mbar_init(&p_full[1], 6);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&pv_done[i], 1);
+      mbar_init(&peer_pv[i], 1);  // arrived by the peer's tensor-core commit
+    }
     mbar_init(mma_done, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&xin_full[i], 1);  // local expect-tx arrival + the peer's bytes
@@ -383,6 +401,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const uint32_t stage_base = smem_u32(smem + OFF_STAGE);
+  const uint32_t p_base = smem_u32(smem + OFF_P);
 
   if (warp == prod_warp) {
     // ------------------------------------------------------------ producer
@@ -447,16 +466,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     }
   } else if (warp == mma_warp) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idS = tc::idesc_bf16(128, TBN, 0, 0);
+    constexpr uint32_t idS = tc::idesc_bf16(128, TBN / 2, 0, 0);
     constexpr uint32_t idPV = tc::idesc_bf16(128, 256, 0, 1);
-    // S of tile n needs its KV stage, the S columns (every softmax thread
-    // has read S of tile n - 1) and, first in a segment, the segment's Q;
-    // P.V of tile n needs P of tile n and, first in a segment, the previous
-    // segment's O read out.  Within a segment the two streams are issued as
-    // soon as each is ready (P.V first), so S runs ahead of the P round trip
-    // between the CTAs.
+    // Half e of S of tile n (ring position q = 2n + e) needs its KV stage,
+    // its TMEM slot (the readers of position q - 3 are done) and, first in
+    // a segment, the segment's Q; P.V of tile n needs P of tile n and, first
+    // in a segment, the previous segment's O read out.  Within a segment the
+    // two streams are issued as soon as each is ready (P.V first), so S
+    // runs ahead of the P round trip between the CTAs.
     bool ok = true;
-    int ns = 0, npv = 0;  // global tile counters
+    int qs = 0, npv = 0;  // global S ring position, global P.V tile counter
     for_each_seg([&](const TcSeg& sg, int k, int n0, const TcSeg*) -> bool {
       const int n1 = n0 + cdiv(sg.end - sg.start, TBN);
       uint64_t t_idle = 0;
@@ -467,21 +486,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         // (lane 0 decides, so the warp stays converged)
         if (!have_o) have_o = __shfl_sync(0xffffffffu, mbar_test(o_free, (k - 1) & 1), 0);
         const bool pv_ready =
-            have_o && __shfl_sync(0xffffffffu, npv < ns && mbar_test(p_full, npv & 1), 0);
+            have_o && __shfl_sync(0xffffffffu,
+                                  npv < (qs >> 1) && mbar_test(&p_full[npv & 1], (npv >> 1) & 1),
+                                  0);
         if (pv_ready) {
           tc::fence_after_sync();
           if (tc::elect_one()) {
-            // A = P (TMEM, 16 tokens = 8 packed columns per step); B = V:
-            // MN-major, 128-byte swizzle (N step = next 64-dim box, K step =
-            // 8 tokens = 1024 B; 16 tokens per MMA = 2048 B = 128 in the
-            // descriptor's address field).
+            // A = P (shared memory, K-major with 128-byte swizzle, 8-row
+            // groups 1024 B apart; 16 tokens = 32 B = 2 in the address
+            // field per step); B = V: MN-major, 128-byte swizzle (N step =
+            // next 64-dim box, K step = 8 tokens = 1024 B; 16 tokens per MMA
+            // = 2048 B = 128 in the address field).
             const uint64_t d0 = tc::smem_desc(stage_base + (npv % TSTAGES) * STAGE_BYTES,
                                               CHUNK_BYTES, 1024, tc::kLayoutSw128);
+            const uint64_t da =
+                tc::smem_desc(p_base + (npv & 1) * P_BYTES, 16, 1024, tc::kLayoutSw128);
 #pragma unroll
             for (int kk = 0; kk < TBN / 16; ++kk)
-              tc::mma_ts(tmem, tmem + P_COL + kk * 8, d0 + static_cast<uint64_t>(kk * 128),
-                         idPV, (npv > n0 || kk > 0) ? 1u : 0u);
-            tc::commit(pv_done);
+              tc::mma_ss(tmem, da + static_cast<uint64_t>(kk * 2),
+                         d0 + static_cast<uint64_t>(kk * 128), idPV,
+                         (npv > n0 || kk > 0) ? 1u : 0u);
+            tc::commit(&pv_done[npv & 1]);
+            // (the peer may then write the P of tile npv + 2 into this
+            // CTA's buffer npv & 1)
+            tc::commit_multicast(&peer_pv[npv & 1], static_cast<uint16_t>(1u << peer));
             tc::commit(&kv_empty[npv % TSTAGES]);
           }
           __syncwarp();
@@ -489,16 +517,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           progress = true;
         }
         if (!have_q) have_q = __shfl_sync(0xffffffffu, mbar_test(q_ready, k & 1), 0);
+        const int ns = qs >> 1, e = qs & 1;  // tile and token half of position qs
         const bool s_ready =
-            have_q && __shfl_sync(0xffffffffu,
-                                  ns < n1 &&
-                                      mbar_test(&kv_full[ns % TSTAGES], (ns / TSTAGES) & 1) &&
-                                      (ns == 0 || mbar_test(s_free, (ns - 1) & 1)),
-                                  0);
+            have_q &&
+            __shfl_sync(0xffffffffu,
+                        ns < n1 && mbar_test(&kv_full[ns % TSTAGES], (ns / TSTAGES) & 1) &&
+                            (qs < 3 || mbar_test(&s_slot_free[qs % 3], ((qs - 3) / 3) & 1)),
+                        0);
         if (s_ready) {
           const int st = ns % TSTAGES;
           const int valid = min(TBN, sg.end - (sg.start + (ns - n0) * TBN));
-          if (valid < TBN) {
+          if (e == 0 && valid < TBN) {
             // Rows past the segment end hold other tokens or NaN: zero their
             // latent part so the P.V product sees 0 * 0 there (their scores
             // are masked; the rope part only enters those scores).
@@ -514,28 +543,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           }
           tc::fence_after_sync();
           if (tc::elect_one()) {
-            // S = Q K^T: A = Q from TMEM (16 dims = 8 packed columns per
-            // step), B = K tile, K-major: the latent chunks with 128-byte
-            // swizzle (8-row groups 1024 B apart), then the rope part with
-            // 64-byte swizzle (groups 512 B apart).  The descriptor's
-            // start-address field (bytes / 16) is advanced by addition: one
-            // 64-dim box is CHUNK_BYTES / 16, one 16-dim step 2.
+            // S half e = Q K^T over tokens [32 e, 32 e + 32): A = Q from
+            // TMEM (16 dims = 8 packed columns per step), B = those 32 K
+            // rows, K-major: the latent chunks with 128-byte swizzle (8-row
+            // groups 1024 B apart, 32 rows = 4096 B), then the rope part with
+            // 64-byte swizzle (groups 512 B apart, 32 rows = 2048 B).  The
+            // descriptor's start-address field (bytes / 16) is advanced by
+            // addition: one 64-dim box is CHUNK_BYTES / 16, one 16-dim step 2.
             const uint32_t sa = stage_base + st * STAGE_BYTES;
-            const uint64_t d0 = tc::smem_desc(sa, 16, 1024, tc::kLayoutSw128);
-            const uint64_t dr = tc::smem_desc(sa + TLAT * CHUNK_BYTES, 16, 512, tc::kLayoutSw64);
+            const uint32_t dS = tmem + S_COL + (qs % 3) * 32;
+            const uint64_t d0 = tc::smem_desc(sa + e * 4096, 16, 1024, tc::kLayoutSw128);
+            const uint64_t dr =
+                tc::smem_desc(sa + TLAT * CHUNK_BYTES + e * 2048, 16, 512, tc::kLayoutSw64);
 #pragma unroll
             for (int ks = 0; ks < TLAT * 4; ++ks)
-              tc::mma_ts(tmem + S_COL, tmem + Q_COL + ks * 8,
+              tc::mma_ts(dS, tmem + Q_COL + ks * 8,
                          d0 + static_cast<uint64_t>((ks >> 2) * (CHUNK_BYTES >> 4) + (ks & 3) * 2),
                          idS, ks > 0 ? 1u : 0u);
 #pragma unroll
             for (int kr = 0; kr < 2; ++kr)
-              tc::mma_ts(tmem + S_COL, tmem + Q_COL + TLAT * 32 + kr * 8,
+              tc::mma_ts(dS, tmem + Q_COL + TLAT * 32 + kr * 8,
                          dr + static_cast<uint64_t>(kr * 2), idS, 1u);
-            tc::commit(s_full);
+            tc::commit(&s_slot_full[qs % 3]);
           }
           __syncwarp();
-          ++ns;
+          ++qs;
           progress = true;
         }
         if (progress) {
@@ -574,15 +606,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     const bool lead = xi == 0 && h == 0;  // registers the expected bytes of each message
     const float scale_log2 = p.sm_scale * kLog2e;
     const uint8_t* xin = smem + OFF_XIN;
-    const uint8_t* pin = smem + OFF_PIN;
-    uint8_t* pout = smem + OFF_POUT;
-    uint8_t* xout = smem + OFF_XOUT;
+    uint8_t* pbuf = smem + OFF_P;
+    const float* ain = reinterpret_cast<const float*>(smem + OFF_AIN);
+    float* aout = reinterpret_cast<float*>(smem + OFF_AOUT);
     float* red = reinterpret_cast<float*>(smem + OFF_RED);  // [2 tiles][2 halves][64]
     float* lred = red + 2 * 2 * 64;                          // [2 halves][64]
-    // The peer's buffers and barriers (messages are st.async stores that
+    // The peer's buffers and barriers (bulk copies and st.async stores
     // complete their bytes on the receiving CTA's barrier).
     const uint32_t xin_peer = tc::map_peer(smem_u32(smem + OFF_XIN), peer);
-    const uint32_t pin_peer = tc::map_peer(smem_u32(smem + OFF_PIN), peer);
+    const uint32_t p_peer = tc::map_peer(p_base, peer);
+    const uint32_t ain_peer = tc::map_peer(smem_u32(smem + OFF_AIN), peer);
     const uint32_t fin_peer = tc::map_peer(smem_u32(smem + OFF_FIN), peer);
     const uint32_t xin_bar_peer0 = tc::map_peer(smem_u32(&xin_full[0]), peer);
     const uint32_t pin_bar_peer0 = tc::map_peer(smem_u32(&pin_full[0]), peer);
@@ -595,13 +628,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     auto own_sync = [&](bool good) -> bool { return named_bar_and(1, 128, good); };
     // This thread's O columns: all 256 on forwarding rows, half on own rows.
     const int o_c0 = own ? 128 * h : 0, o_c1 = own ? 128 * h + 128 : 256;
+    // P.V of tile m has completed.  pv_done[m & 1] completes once per two
+    // tiles; every caller waits for m before P.V of m + 2 can have been
+    // issued, so the parity is never two phases behind.
+    auto pv_wait = [&](int m) -> bool { return warp_wait(&pv_done[m & 1], (m >> 1) & 1); };
 
     // Rescales this thread's O columns by alpha once the previous P.V has
     // completed; warp-uniform (lanes with alpha = 1 keep their values).  Not
     // needed on a segment's first tile (O is empty).
     auto rescale_o = [&](int n, int n0, float alpha) -> bool {
       if (n == n0 || !__any_sync(0xffffffffu, alpha != 1.f)) return true;
-      if (!warp_wait(pv_done, (n - 1) & 1)) return false;
+      if (!pv_wait(n - 1)) return false;
       tc::fence_after_sync();
 #pragma unroll 1
       for (int c = o_c0; c < o_c1; c += 32) {
@@ -616,23 +653,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       tc::wait_st();
       return true;
     };
-    auto p_ready = [&]() {
-      tc::wait_st();
+    // This warp's part of tile n's P.V inputs is in place (its O rows
+    // rescaled, its P rows written and made visible to the async proxy).
+    // One barrier per tile parity: a warp's arrival for tile n + 2 comes
+    // after P.V of tile n has completed (owners wait for it before writing
+    // P; forwarders before sending the scores P answers), so the phases of
+    // one barrier never mix two tiles.
+    auto p_ready = [&](int n) {
       tc::fence_before_sync();
-      mbar_arrive(p_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[n & 1]);
     };
-    auto s_done = [&]() {
+    // S ring position q: its slot's columns, wait and release.
+    auto s_col = [&](int q) -> uint32_t { return tmem + lane_base + S_COL + (q % 3) * 32; };
+    auto s_test = [&](int q) -> bool { return mbar_test(&s_slot_full[q % 3], (q / 3) & 1); };
+    auto s_done = [&](int q) {
       tc::wait_ld();
       tc::fence_before_sync();
-      mbar_arrive(s_free);
+      mbar_arrive(&s_slot_free[q % 3]);
     };
 
     // ---- Q of a segment: this thread's vector, the CTA's latent dims (four
     // 64-dim chunks) and then its 32 rope dims, into TMEM lane row_i as
     // packed bf16 pairs (padding vectors are zeros); on own rows one warp
     // takes chunks 0-1, the other chunks 2-3 and the rope part.  Called once
-    // the previous segment's S products, which read Q, are complete (this
-    // thread has loaded all of them).
+    // the previous segment's S products, which read Q, are complete.
     auto load_q = [&](const TcSeg& sg) {
       const int v = sg.g * 128 + row_i;
       const bool valid_v = v < nvec;
@@ -707,72 +752,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       float m_used = -INFINITY, l_run = 0.f;
 
       if (!own) {
-        // Forwarding rows.  Each warp stores the P of tile np as soon as it
-        // has come back (first: it gates the P.V that frees a KV stage) and
-        // sends its rows' partial scores of tile ns as soon as S is there.
-        // Partial ns goes into the peer's buffer ns & 1, which the peer has
-        // read once it returned the P of tile ns - 2: hence ns <= np + 1.
-        int ns = n0, np = n0;
+        // Forwarding rows.  Each warp handles the P of tile np as soon as
+        // it has come back (first: it gates the P.V that frees a KV stage;
+        // only the rescale factors are read, P itself is the MMA's operand
+        // in place) and sends its rows' partial scores of tile ns as soon as
+        // S is there.  ns <= np + 1 keeps the answer barrier of tile ns - 2
+        // observed before it is armed again, and the rescale factors of
+        // tile ns - 2 read before the peer can send those of tile ns.
+        const int fw = xi >> 5;  // which of the two forwarding warps
+        uint8_t* xo = smem + OFF_XOUT + fw * (XS_PLANE / 2);
+        int fq = 2 * n0, np = n0;  // next S ring position to forward, next P tile
         uint64_t t_idle = 0;
         uint32_t spins = 0;
         while (np < n1) {
           bool did = false;
-          if (np < ns &&
+          if (np < (fq >> 1) &&
               __shfl_sync(0xffffffffu, tc::mbar_test_cluster(&pin_full[np & 1], (np >> 1) & 1),
                           0)) {
-            const uint8_t* src = pin + (np & 1) * XP_BYTES;
-            uint32_t pk[32];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint4 x = *reinterpret_cast<const uint4*>(src + xoff(xi, j, XP_ROW));
-              pk[4 * j] = x.x;
-              pk[4 * j + 1] = x.y;
-              pk[4 * j + 2] = x.z;
-              pk[4 * j + 3] = x.w;
-            }
-            const float alpha = reinterpret_cast<const float*>(src + XP_ALPHA)[xi];
+            const float alpha = ain[(np & 1) * 64 + xi];
             if (!rescale_o(np, n0, alpha)) { ok = false; break; }
-            // P's columns are free once the previous P.V has completed
-            if (np >= 1 && !warp_wait(pv_done, (np - 1) & 1)) { ok = false; break; }
-            tc::fence_after_sync();
-            tc::st_32x32b_x32(tmem + lane_base + P_COL, pk);
-            p_ready();
+            p_ready(np);
             ++np;
             did = true;
           }
-          if (ns < n1 && ns <= np + 1 &&
-              __shfl_sync(0xffffffffu, mbar_test(s_full, ns & 1), 0)) {
+          const int ns = fq >> 1, e = fq & 1;  // tile and token half of position fq
+          if (ns < n1 && ns <= np + 1 && __shfl_sync(0xffffffffu, s_test(fq), 0)) {
             tc::fence_after_sync();
-            uint32_t sr[64];
-            tc::ld_32x32b_x32(tmem + lane_base + S_COL,
-                              *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tc::ld_32x32b_x32(tmem + lane_base + S_COL + 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-            s_done();
+            uint32_t sr[32];
+            tc::ld_32x32b_x32(s_col(fq), sr);
+            s_done(fq);
             tc::reg_fence(sr);
             const int bb = ns & 1;
-            if (lead) mbar_arrive_expect_tx(&pin_full[bb], XP_BYTES);  // P of tile ns
-            // The warp's 32 rows go to the peer as one bulk copy of a local
-            // copy (its previous copy has read that buffer first).
-            const uint32_t base = (xi & ~31u) * XS_ROW;
+            if (e == 0 && lead) mbar_arrive_expect_tx(&pin_full[bb], P_HALF + 256);  // P of ns
+            // The warp's 32 rows of this token half (plane e) are staged in
+            // its 4 KiB buffer (once the previous plane's copy has read it)
+            // and handed to the peer as one bulk copy; scaled by sm_scale *
+            // log2(e), so that the owner's sum is one fused multiply-add.
             if (lane == 0) tc::bulk_wait_read();
             __syncwarp();
-            // (sent scaled by sm_scale * log2(e): the owner's sum is then
-            // one fused multiply-add)
-            auto scaled = [&](int k) {
-              return __float_as_uint(__uint_as_float(sr[k]) * scale_log2);
-            };
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              *reinterpret_cast<uint4*>(xout + xoff(xi, j, XS_ROW)) =
-                  make_uint4(scaled(4 * j), scaled(4 * j + 1), scaled(4 * j + 2),
-                             scaled(4 * j + 3));
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(xo + xoff(xi & 31, j, 128)) = make_uint4(
+                  __float_as_uint(__uint_as_float(sr[4 * j]) * scale_log2),
+                  __float_as_uint(__uint_as_float(sr[4 * j + 1]) * scale_log2),
+                  __float_as_uint(__uint_as_float(sr[4 * j + 2]) * scale_log2),
+                  __float_as_uint(__uint_as_float(sr[4 * j + 3]) * scale_log2));
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
-              tc::bulk_copy_to_peer(xin_peer + bb * XS_BYTES + base, xout + base, 32 * XS_ROW,
-                                    xin_bar_peer0 + bb * 8);
-            ++ns;
+              tc::bulk_copy_to_peer(xin_peer + bb * XS_BYTES + e * XS_PLANE + fw * 32 * 128, xo,
+                                    32 * 128, xin_bar_peer0 + bb * 8);
+            ++fq;
             did = true;
           }
           if (did) {
@@ -797,16 +827,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           uint32_t sr[32];
           float mt = -INFINITY;
           // ---- this half's 32 partial scores
-          if (!bad && warp_wait(s_full, n & 1)) {
+          const int q = 2 * n + h;  // S ring position of this half
+          if (!bad && warp_wait(&s_slot_full[q % 3], (q / 3) & 1)) {
             tc::fence_after_sync();
-            tc::ld_32x32b_x32(tmem + lane_base + S_COL + 32 * h, sr);
-            s_done();
+            tc::ld_32x32b_x32(s_col(q), sr);
+            s_done(q);
             tc::reg_fence(sr);
             // ---- add the peer's partial scores for them (xin[bb] is not
             // rewritten before the peer has received this tile's P)
             if (lead) mbar_arrive_expect_tx(&xin_full[bb], XS_BYTES);
             if (warp_wait_cluster(&xin_full[bb], u)) {
-              const uint8_t* src = xin + bb * XS_BYTES;
+              const uint8_t* src = xin + bb * XS_BYTES + h * XS_PLANE;  // this half's plane
               const int valid = min(TBN, sg.end - (sg.start + (n - n0) * TBN)) - 32 * h;
               // x = (own partial + peer partial) * sm_scale * log2(e), the
               // peer's part arriving scaled; tokens past the segment end
@@ -814,8 +845,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
               auto add_partials = [&](auto masked) {
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
-                  const float4 t =
-                      *reinterpret_cast<const float4*>(src + xoff(xi, 8 * h + j4, XS_ROW));
+                  const float4 t = *reinterpret_cast<const float4*>(src + xoff(xi, j4, 128));
                   const float tv[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
                   for (int e = 0; e < 4; ++e) {
@@ -841,8 +871,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           // other half reads this tile's value before either writes the
           // tile after next's)
           red[(bb * 2 + h) * 64 + xi] = mt;
-          // (the outbound P buffer is free once the previous tile's bulk copy
-          // has read it; its issuing thread checks before this barrier)
+          // The P buffer of parity bb: P.V of tile n - 2 has read this CTA's
+          // half of it, and the peer's P.V of tile n - 2 its half in the
+          // peer, where this tile's copy goes (checked here, where the wait
+          // overlaps the others' arrival at the meeting).  The previous
+          // tile's bulk copies have read this CTA's P rows and factors.
+          if (n >= 2 && !bad && !pv_wait(n - 2)) bad = true;
+          if (h == 0 && xi < 32 && n >= 2 && !bad &&
+              !warp_wait_cluster(&peer_pv[bb], ((n - 2) >> 1) & 1))
+            bad = true;
           if (lead) tc::bulk_wait_read();
           if (!own_sync(!bad)) { ok = false; break; }
           mt = fmaxf(red[(bb * 2) * 64 + xi], red[(bb * 2 + 1) * 64 + xi]);
@@ -865,31 +902,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             pk[j] = pack_bf16x2(a0, a1);
           }
           l_run += (psum[0] + psum[1]) + (psum[2] + psum[3]);
-          // ---- this half of P, and alpha, to the peer for its half of O
-          // (its buffer bb held the P of tile n - 2, which it has stored: it
-          // sent this tile's partial scores only afterwards).  The 128 owner
-          // threads write their parts into the outbound buffer and one of
-          // them hands the 64 rows to the peer as one bulk copy, which runs
-          // in the background: per-thread remote stores stalled the owners
-          // behind the partial-score traffic in flight.
+          // ---- this half of P into the P buffer of tile parity bb (its
+          // rows of this CTA); then the 64 rows and the rescale factors go
+          // to the same place in the peer's buffer as one bulk copy each,
+          // which run in the background.
+          uint8_t* pdst = pbuf + bb * P_BYTES + rank * P_HALF;
           {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4*>(pout + xoff(xi, 4 * h + j, XP_ROW)) =
+              *reinterpret_cast<uint4*>(pdst + xoff(xi, 4 * h + j, 128)) =
                   make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-            if (h == 0) reinterpret_cast<float*>(pout + XP_ALPHA)[xi] = alpha;
-            fence_proxy_async_smem();  // the bulk copy reads through the async proxy
+            if (h == 0) aout[xi] = alpha;
+            fence_proxy_async_smem();  // read by the MMA and the bulk copies
           }
           own_sync(true);  // (no wait since the last meeting)
-          if (lead)
-            tc::bulk_copy_to_peer(pin_peer + bb * XP_BYTES, pout, XP_BYTES, pin_bar_peer0 + bb * 8);
-          if (!rescale_o(n, n0, alpha) || (n >= 1 && !warp_wait(pv_done, (n - 1) & 1))) {
+          if (lead) {
+            tc::bulk_copy_to_peer(p_peer + bb * P_BYTES + rank * P_HALF, pdst, P_HALF,
+                                  pin_bar_peer0 + bb * 8);
+            tc::bulk_copy_to_peer(ain_peer + bb * 256, aout, 256, pin_bar_peer0 + bb * 8);
+          }
+          if (!rescale_o(n, n0, alpha)) {
             bad = true;  // the next meeting ends the loop
             continue;
           }
-          tc::fence_after_sync();
-          tc::st_32x32b_x16(tmem + lane_base + P_COL + 16 * h, pk);
-          p_ready();
+          p_ready(n);
         }
         // ---- row sum over both halves (all four warps leave the loop
         // together, so all four come here; a failure in the last tile's
@@ -922,11 +958,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       }
       if (!ok) return false;
       // ---- the next segment's Q first, so that its S products start while
-      // this segment's O is read out
-      if (next) load_q(*next);
+      // this segment's O is read out.  Every S half reads all of Q: the
+      // own-row warps of the first token half, which read no second half,
+      // first wait for the last tile's second half to complete.
+      bool q_ok = true;
+      if (next) {
+        if (own && h == 0) {
+          const int ql = 2 * (n1 - 1) + 1;
+          q_ok = warp_wait(&s_slot_full[ql % 3], (ql / 3) & 1);
+        }
+        if (q_ok) load_q(*next);
+      }
       // ---- epilogue: this thread's O columns (normalised) and, from the
       // owner, lse
-      const bool pv_ok = warp_wait(pv_done, (n1 - 1) & 1);
+      const bool pv_ok = pv_wait(n1 - 1) && q_ok;
       if ((own && !own_sync(pv_ok)) || !pv_ok) {  // the owners leave together
         ok = false;
         return false;

@@ -75,6 +75,15 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
       "[%0];" ::"r"(smem_u32(bar))
       : "memory");
 }
+// The same arrival on the barrier at `bar`'s offset in each CTA of the
+// cluster whose bit is set in `cta_mask`.
+__device__ __forceinline__ void commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
 
 // ------------------------------------------------------------ TMEM <-> regs
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane
