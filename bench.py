@@ -165,7 +165,7 @@ def _roofline(w, args, workload, deterministic, kv_bytes, flops, s1_ms):
     # the stage-1 kernel the library picks: a tcgen05 kernel (R = 512 bf16:
     # CTA pairs; R = 256 bf16 or fp8: one CTA) from 64 query vectors per
     # sequence, warp MMA otherwise
-    tc = (R == 256 or not w.kv_fp8) and w.rows_per_seq * H >= 64 and args.path != 1
+    tc = (R == 256 or not w.kv_fp8) and w.rows_per_seq * H > 32 and args.path != 1
     tc = tc or args.path == 2
     kernel_src = ("decode_tc1.cu" if R == 256 else "decode_tc.cu") if tc else "decode_mma.cu"
     traffic = _traffic_record(os.path.join(ROOT, "mla_paged_kv_concat_gb300", "csrc",

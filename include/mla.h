@@ -65,9 +65,11 @@ typedef enum {
 typedef enum {
   MLA_PATH_AUTO = 0,
   MLA_PATH_MMA_SYNC = 1, /* warp-level bf16 MMA: every cache type and shape   */
-  MLA_PATH_TCGEN05 = 2   /* tcgen05/TMEM, 2-CTA clusters of 128 query vectors:
-                            bf16 cache with kv_lora_rank 512; AUTO takes it
-                            from 128 query vectors (rows x heads) per sequence */
+  MLA_PATH_TCGEN05 = 2   /* tcgen05/TMEM, 128 query vectors per 2-CTA cluster
+                            (bf16 cache, kv_lora_rank 512) or per CTA
+                            (kv_lora_rank 256, bf16 or fp8 cache); AUTO takes
+                            it above 32 query vectors (rows x heads) per
+                            sequence */
 } mla_decode_path;
 
 /*

@@ -404,18 +404,20 @@ mla_status prepare_decode(const void* q, int64_t q_row_stride,
 }
 
 // Stage-1 kernel choice: a tcgen05 kernel when forced, or (AUTO) when one
-// supports the cache and the sequences have at least 64 query vectors for
+// supports the cache and the sequences have more than 32 query vectors for
 // its M = 128 tile; the warp-MMA kernel otherwise.  Measured on GB300
 // (32 sequences of 8192 tokens, stage 1 alone): the warp-MMA kernel's time
-// grows with the query vectors (its fragment loads from shared memory bound
-// it), the tcgen05 kernels' hardly; they tie near 32 vectors and the
-// tcgen05 kernels lead from 64 (R = 512 bf16: 128 against 143 us; R = 256:
-// 57 against 98 us bf16, 71 against 131 us E4M3) to 128 (2.0-3.3 x).
+// steps up with its 16- or 32-vector units (its fragment loads from shared
+// memory bound it), the tcgen05 kernels' hardly moves; at 32 vectors the
+// warp-MMA kernel is ahead by 3-20 % (R = 512: 80 against 101 us; R = 256:
+// 53 against 55 us bf16, 67 against 70 us E4M3), from 40 vectors on the
+// tcgen05 kernels lead by 1.4-2.4 x (R = 512 at 48: 102 against 142 us;
+// R = 256 at 40: 55 against 110 us bf16, 69 against 139 us E4M3).
 bool use_tc(const mla::DecodeParams& p, bool fp8, int R, mla_decode_path path) {
   if (path == MLA_PATH_TCGEN05) return true;
   if (path == MLA_PATH_MMA_SYNC) return false;
   const int64_t nvec = static_cast<int64_t>(p.rows_per_seq) * p.num_heads;
-  return tc_supported(fp8, R) && nvec >= 64;
+  return tc_supported(fp8, R) && nvec > 32;
 }
 
 // Everything stage 1 needs at launch time, computed once per call (or once

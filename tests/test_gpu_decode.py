@@ -94,7 +94,7 @@ def test_full_head_deterministic_single_pass(cuda_dev):
 @pytest.mark.parametrize("path", [mla.MLA_PATH_AUTO] + PATHS)
 def test_fp8_small(cuda_dev, path):
     """B=32, H=32, E4M3 cache with R=256 at the benchmark's split count, on
-    both stage-1 kernels (AUTO takes the warp-MMA kernel below 64 query
+    both stage-1 kernels (AUTO takes the warp-MMA kernel at 32 query
     vectors): the first and last vector of every (sequence, 32-vector) unit
     (each sequence is one 128-vector unit of the tcgen05 schedule), plus
     random pairs."""
