@@ -36,8 +36,9 @@
 //              owns are forwarded by the two warps of their lane quarters
 //              (partial scores out, the rescale factors of returned P in,
 //              whichever is ready); the 64 this CTA owns get four warps,
-//              two per lane quarter, each taking one half of the 64 tokens,
-//              which share the row maximum and sum through shared memory
+//              two per lane quarter, each taking one half of the 64 tokens;
+//              the two of a quarter share the row maximum and sum through
+//              shared memory and send the quarter's P rows to the peer
 //              (lazy rescaling of O only when the running max grows by more
 //              than 2^8);
 //   one warp   MMA issuer (one elected thread) and TMEM owner;
@@ -604,6 +605,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     const int h = warp >> 2;        // token half (own rows); 0 on forwarding warps
     const int xi = row_i & 63;      // row within the 64-vector exchange blocks
     const bool lead = xi == 0 && h == 0;  // registers the expected bytes of each message
+    // (own rows) the lane quarter among the CTA's two, and the thread that
+    // sends that quarter's P rows and rescale factors to the peer
+    const int oq = xi >> 5;
+    const bool qlead = own && h == 0 && (xi & 31) == 0;
     const float scale_log2 = p.sm_scale * kLog2e;
     const uint8_t* xin = smem + OFF_XIN;
     uint8_t* pbuf = smem + OFF_P;
@@ -621,11 +626,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     const uint32_t pin_bar_peer0 = tc::map_peer(smem_u32(&pin_full[0]), peer);
     const uint32_t fin_bar_peer = tc::map_peer(smem_u32(fin_full), peer);
     bool ok = true;
-    // Meeting of the four warps of this CTA's own rows (named barrier 1),
-    // which also ANDs their flags.  Every wait of theirs is bounded, so each
-    // reaches every meeting; one that gave up on a wait passes false, and
-    // all four take the same exit after the meeting.
-    auto own_sync = [&](bool good) -> bool { return named_bar_and(1, 128, good); };
+    // Meeting of the two warps (one per token half) of a lane quarter of
+    // this CTA's own rows (named barrier 1 or 2), which also ANDs their
+    // flags.  Every wait of theirs is bounded, so each reaches every
+    // meeting; one that gave up on a wait passes false, and both take the
+    // same exit after the meeting.  The two quarters share no data and move
+    // on independently.
+    auto own_sync = [&](bool good) -> bool { return named_bar_and(1 + oq, 64, good); };
     // This thread's O columns: all 256 on forwarding rows, half on own rows.
     const int o_c0 = own ? 128 * h : 0, o_c1 = own ? 128 * h + 128 : 256;
     // P.V of tile m has completed.  pv_done[m & 1] completes once per two
@@ -877,10 +884,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           // overlaps the others' arrival at the meeting).  The previous
           // tile's bulk copies have read this CTA's P rows and factors.
           if (n >= 2 && !bad && !pv_wait(n - 2)) bad = true;
-          if (h == 0 && xi < 32 && n >= 2 && !bad &&
-              !warp_wait_cluster(&peer_pv[bb], ((n - 2) >> 1) & 1))
+          if (h == 0 && n >= 2 && !bad && !warp_wait_cluster(&peer_pv[bb], ((n - 2) >> 1) & 1))
             bad = true;
-          if (lead) tc::bulk_wait_read();
+          if (qlead) tc::bulk_wait_read();
           if (!own_sync(!bad)) { ok = false; break; }
           mt = fmaxf(red[(bb * 2) * 64 + xi], red[(bb * 2 + 1) * 64 + xi]);
           // ---- online softmax with lazy rescaling (both halves take the
@@ -903,9 +909,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           }
           l_run += (psum[0] + psum[1]) + (psum[2] + psum[3]);
           // ---- this half of P into the P buffer of tile parity bb (its
-          // rows of this CTA); then the 64 rows and the rescale factors go
-          // to the same place in the peer's buffer as one bulk copy each,
-          // which run in the background.
+          // rows of this CTA); then the quarter's 32 rows and rescale
+          // factors go to the same place in the peer's buffer as one bulk
+          // copy each, which run in the background.
           uint8_t* pdst = pbuf + bb * P_BYTES + rank * P_HALF;
           {
 #pragma unroll
@@ -916,10 +922,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             fence_proxy_async_smem();  // read by the MMA and the bulk copies
           }
           own_sync(true);  // (no wait since the last meeting)
-          if (lead) {
-            tc::bulk_copy_to_peer(p_peer + bb * P_BYTES + rank * P_HALF, pdst, P_HALF,
+          if (qlead) {
+            tc::bulk_copy_to_peer(p_peer + bb * P_BYTES + rank * P_HALF + oq * (P_HALF / 2),
+                                  pdst + oq * (P_HALF / 2), P_HALF / 2, pin_bar_peer0 + bb * 8);
+            tc::bulk_copy_to_peer(ain_peer + bb * 256 + oq * 128, aout + oq * 32, 128,
                                   pin_bar_peer0 + bb * 8);
-            tc::bulk_copy_to_peer(ain_peer + bb * 256, aout, 256, pin_bar_peer0 + bb * 8);
           }
           if (!rescale_o(n, n0, alpha)) {
             bad = true;  // the next meeting ends the loop
@@ -927,8 +934,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           }
           p_ready(n);
         }
-        // ---- row sum over both halves (all four warps leave the loop
-        // together, so all four come here; a failure in the last tile's
+        // ---- row sum over both halves (both warps of a quarter leave the
+        // loop together, so both come here; a failure in the last tile's
         // second half shows at this meeting)
         if (ok) {
           lred[h * 64 + xi] = l_run;
@@ -937,7 +944,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         }
         // the last copy has read the outbound buffer before this CTA can
         // leave (the next segment's first tile waits for it anyway)
-        if (lead) tc::bulk_wait_read();
+        if (qlead) tc::bulk_wait_read();
       }
 
       // ---- the owner's 1 / l reaches the other CTA as the segment's last
@@ -972,7 +979,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       // ---- epilogue: this thread's O columns (normalised) and, from the
       // owner, lse
       const bool pv_ok = pv_wait(n1 - 1) && q_ok;
-      if ((own && !own_sync(pv_ok)) || !pv_ok) {  // the owners leave together
+      if ((own && !own_sync(pv_ok)) || !pv_ok) {  // a quarter's owners leave together
         ok = false;
         return false;
       }
