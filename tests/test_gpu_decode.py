@@ -345,3 +345,26 @@ def test_many_splits_on_short_sequences(cuda_dev, path):
     H = 16 if path == mla.MLA_PATH_MMA_SYNC else 128
     w = W.make_workload("shortS", seed=78, seq_lens=[1, 64, 65, 200, 0], num_heads=H)
     _run(w, 2 * sm_count(), path)
+
+
+@pytest.mark.parametrize("R,fp8", [(512, False), (256, False), (256, True), (512, True)])
+@pytest.mark.parametrize("H,rows", [(32, 1), (33, 1), (16, 2), (17, 2)])
+def test_auto_kernel_choice(cuda_dev, R, fp8, H, rows):
+    """AUTO runs the tcgen05 kernel above 32 query vectors per sequence when
+    one covers the cache (R = 512 bf16, R = 256 bf16 or fp8) and the
+    warp-MMA kernel otherwise: its result is bitwise that of the forced
+    choice, and it meets the decode bar against the oracle."""
+    w = W.make_workload("auto", seed=41 + H + R, seq_lens=[700, 130, 1], num_heads=H,
+                        kv_lora_rank=R, rows_per_seq=rows,
+                        **(dict(kv_fp8=True, kv_scale=0.05, write="all") if fp8 else {}))
+    S = 4
+    d = Dev(w)
+    d.write()
+    o_auto, l_auto = d.decode(S, path=mla.MLA_PATH_AUTO)
+    tc = H * rows > 32 and (R == 256 or not fp8)
+    o_ref_path, l_ref_path = d.decode(S, path=mla.MLA_PATH_TCGEN05 if tc else mla.MLA_PATH_MMA_SYNC)
+    torch.cuda.synchronize()
+    assert torch.equal(o_auto.view(torch.int16), o_ref_path.view(torch.int16))
+    assert torch.equal(l_auto, l_ref_path)
+    o_ref, lse_ref = oracle_decode(w, oracle_cache(w))
+    assert_close(o_auto, l_auto, o_ref, lse_ref, what=f"AUTO H={H} rows={rows} R={R} fp8={fp8}")
