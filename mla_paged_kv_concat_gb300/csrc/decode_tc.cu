@@ -840,10 +840,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             tc::ld_32x32b_x32(s_col(q), sr);
             s_done(q);
             tc::reg_fence(sr);
+            // The P buffer of parity bb: P.V of tile n - 2 has read this
+            // CTA's half of it, and the peer's P.V of tile n - 2 its half in
+            // the peer, where this tile's copy goes (checked before the wait
+            // for the peer's partial scores, which it overlaps).
+            if (n >= 2 && !pv_wait(n - 2)) bad = true;
+            if (!bad && h == 0 && n >= 2 &&
+                !warp_wait_cluster(&peer_pv[bb], ((n - 2) >> 1) & 1))
+              bad = true;
             // ---- add the peer's partial scores for them (xin[bb] is not
             // rewritten before the peer has received this tile's P)
             if (lead) mbar_arrive_expect_tx(&xin_full[bb], XS_BYTES);
-            if (warp_wait_cluster(&xin_full[bb], u)) {
+            if (!bad && warp_wait_cluster(&xin_full[bb], u)) {
               const uint8_t* src = xin + bb * XS_BYTES + h * XS_PLANE;  // this half's plane
               const int valid = min(TBN, sg.end - (sg.start + (n - n0) * TBN)) - 32 * h;
               // x = (own partial + peer partial) * sm_scale * log2(e), the
@@ -878,14 +886,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           // other half reads this tile's value before either writes the
           // tile after next's)
           red[(bb * 2 + h) * 64 + xi] = mt;
-          // The P buffer of parity bb: P.V of tile n - 2 has read this CTA's
-          // half of it, and the peer's P.V of tile n - 2 its half in the
-          // peer, where this tile's copy goes (checked here, where the wait
-          // overlaps the others' arrival at the meeting).  The previous
-          // tile's bulk copies have read this CTA's P rows and factors.
-          if (n >= 2 && !bad && !pv_wait(n - 2)) bad = true;
-          if (h == 0 && n >= 2 && !bad && !warp_wait_cluster(&peer_pv[bb], ((n - 2) >> 1) & 1))
-            bad = true;
+          // (the previous tile's bulk copies have read this quarter's P rows
+          // and factors)
           if (qlead) tc::bulk_wait_read();
           if (!own_sync(!bad)) { ok = false; break; }
           mt = fmaxf(red[(bb * 2) * 64 + xi], red[(bb * 2 + 1) * 64 + xi]);
