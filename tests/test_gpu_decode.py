@@ -368,3 +368,24 @@ def test_auto_kernel_choice(cuda_dev, R, fp8, H, rows):
     assert torch.equal(l_auto, l_ref_path)
     o_ref, lse_ref = oracle_decode(w, oracle_cache(w))
     assert_close(o_auto, l_auto, o_ref, lse_ref, what=f"AUTO H={H} rows={rows} R={R} fp8={fp8}")
+
+
+@pytest.mark.parametrize("H,R,fp8,path", [
+    (128, 512, False, mla.MLA_PATH_TCGEN05),
+    (128, 256, True, mla.MLA_PATH_TCGEN05),
+    (16, 512, False, mla.MLA_PATH_MMA_SYNC),
+])
+def test_more_units_than_the_persistent_schedule_holds(cuda_dev, H, R, fp8, path):
+    """520 sequences of one vector block each: more (sequence, block) units
+    than the persistent schedules hold (512), so stage 1 runs as a grid of
+    (block, split group) CTAs (pairs) with S = 4.  Lengths 1..300, some of
+    them shorter than a split.  The first and last vector of every unit and
+    random pairs against the oracle."""
+    from _helpers import unit_pairs
+    rng = np.random.default_rng(77)
+    lens = rng.integers(1, 301, size=520)
+    kw = dict(kv_fp8=True, kv_scale=0.05, write="all") if fp8 else {}
+    w = W.make_workload("grid", seed=78 + H + R, seq_lens=lens, num_heads=H, kv_lora_rank=R,
+                        **kw)
+    pairs = unit_pairs(w, 128 if H == 128 else 16, extra=64, seed=3)
+    _run(w, 4, path, pairs=pairs)
