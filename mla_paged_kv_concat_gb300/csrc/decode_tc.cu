@@ -664,8 +664,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     // rescaled, its P rows written and made visible to the async proxy).
     // One barrier per tile parity: a warp's arrival for tile n + 2 comes
     // after P.V of tile n has completed (owners wait for it before writing
-    // P; forwarders before sending the scores P answers), so the phases of
-    // one barrier never mix two tiles.
+    // P; forwarders arrive once the peer's P of tile n + 2 has landed, which
+    // the peer sends only after this CTA's tensor core signalled that P.V),
+    // so the phases of one barrier never mix two tiles.
     auto p_ready = [&](int n) {
       tc::fence_before_sync();
       __syncwarp();
