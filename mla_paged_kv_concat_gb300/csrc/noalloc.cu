@@ -41,7 +41,7 @@ std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
 unsigned long long g_ctx_id[kMaxDevices] = {};
 
-// Unique id of the current context (0 when the driver cannot say; then
+// Unique id of the current context (0 when the CUDA driver cannot say; then
 // the address is looked up on every call).
 unsigned long long current_context_id() {
   static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
