@@ -271,12 +271,7 @@ __device__ __forceinline__ bool elect_one() {
   return p != 0;
 }
 
-}  // namespace tc
-}  // namespace mla
-
-namespace mla {
-namespace tc {
-
+// ------------------------------------------------------------ bulk copies
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
 // from this CTA's shared memory to a cluster peer's, completing the bytes
 // on the peer's mbarrier (cluster addresses from map_peer); one thread.
